@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of ART decode attention on one decode workload.
+
+One step = one art_decode call (memset of the workspace header, the plan
+kernel, the persistent decode kernel) over the whole batch, inputs resident
+in HBM. Prints one JSON line (rank 0) with queries/s, the HBM roofline of the
+decode kernel, the dense twin, the CPU oracle baseline, clocks and an
+end-to-end figure through the public API with host buffers.
+
+Default workload: the Llama-3-8B-shaped decode layer (batch 16, 32 query /
+8 KV heads, d=128, 32768-token context, bf16, KV block 64, planted keys,
+sink-first most-recent-first order, eps 1e-3, patience 2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 1..5] [--eps E] [--patience P] [--no-cpu-baseline]
+Under torchrun (N > 1) every rank runs its own independently seeded copy of
+the workload (weak scaling, no collective on the data path); the timing is
+the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--eps", type=float, default=None)
+    ap.add_argument("--patience", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (algorithmic bytes of one call)
+# ---------------------------------------------------------------------------
+def listed_blocks(w):
+    """Per item: the listed logical blocks (list of arrays)."""
+    lens = w.visit_lengths()
+    out = []
+    for it in range(w.num_items):
+        b, g = divmod(it, w.num_kv_heads)
+        if w.visit_order is None:
+            out.append(np.arange(lens[it]))
+        else:
+            out.append(w.visit_order[b, g, : lens[it]].astype(np.int64))
+    return out
+
+
+def kv_bytes(w, blocks_used=None):
+    """K+V bytes of the first blocks_used listed blocks of every item (all if None):
+    tokens x 2 (K and V) x head_dim x element size."""
+    per_tok = 2 * w.head_dim * w.elem_bytes
+    tot = 0
+    for it, lst in enumerate(listed_blocks(w)):
+        b = it // w.num_kv_heads
+        k = len(lst) if blocks_used is None else max(0, int(blocks_used[it]))
+        c = lst[:k]
+        toks = np.minimum(w.block_size, int(w.seq_lens[b]) - c * w.block_size).sum()
+        tot += int(toks) * per_tok
+    return tot
+
+
+def side_bytes(w):
+    """q, out, lists and table entries the call reads or writes besides K/V."""
+    qo = 2 * w.batch * w.num_q_heads * w.head_dim * w.elem_bytes
+    lists = 0 if w.visit_order is None else w.visit_order.nbytes
+    pages = int(np.ceil(w.seq_lens / w.page_size).sum()) * 4
+    return qo + lists + pages + w.seq_lens.nbytes + w.num_items * 8
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": float(np.median(power)) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_cache_early_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def load_traffic(config_name):
+    """DRAM bytes per launch of the decode kernel from a committed ncu summary,
+    only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    d = json.load(open(p))
+    e = d.get(config_name)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None, None
+    return e.get("dram_bytes_per_launch"), e
+
+
+def cpu_baseline(w, eps, p, budget_s=12.0):
+    """The CPU oracle on the host cores: whole workload, repeated while under budget."""
+    import oracle as O
+    times = []
+    t_all = time.time()
+    nt = 0
+    while True:
+        t0 = time.time()
+        r = O.run_workload(w, eps_mag=eps, eps_dir=eps, patience=p)
+        times.append(time.time() - t0)
+        nt = r["threads"]
+        if time.time() - t_all > budget_s or len(times) >= 5:
+            break
+    t = float(np.median(times))
+    q = w.batch * w.num_q_heads
+    return {"value": q / t, "unit": "queries/s", "cores": int(nt), "kind": "oracle",
+            "sample": f"whole workload ({w.num_items} items, fp64 C oracle, ART rule), median of {len(times)} runs",
+            "seconds_per_run": t}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle timed as it stands on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    w = W.config(args.config, eps=args.eps, patience=args.patience)
+    eps, p = w.eps_mag, w.patience
+    import oracle as O
+    # each step: the oracle over a bounded sample of items (at most ~10 s per step)
+    n_items = w.num_items
+    t0 = time.time()
+    O.run_workload(w, items=np.arange(min(n_items, 8)), eps_mag=eps, eps_dir=eps, patience=p)
+    per_item = max((time.time() - t0) / min(n_items, 8), 1e-6)
+    k = int(max(1, min(n_items, 10.0 / per_item)))
+    items = np.arange(k)
+    for _ in range(args.warmup):
+        O.run_workload(w, items=items[: max(1, k // 8)], eps_mag=eps, eps_dir=eps, patience=p)
+    ts = []
+    nt = 0
+    for _ in range(args.steps):
+        t0 = time.time()
+        r = O.run_workload(w, items=items, eps_mag=eps, eps_dir=eps, patience=p)
+        ts.append(time.time() - t0)
+        nt = r["threads"]
+    t = float(np.mean(ts))
+    value = k * w.group / t
+    line = {"metric": "decode-attention queries/s (ART)", "value": value, "unit": "queries/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "items_per_step": int(k), "eps": eps, "patience": p},
+            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": int(nt), "kind": "oracle",
+                             "sample": f"{k} of {n_items} (sequence, KV head) items per step"},
+            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import kv_cache_early_gb300 as K
+    from kv_cache_early_gb300 import build as B
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    B.build()
+    w = W.config(args.config, eps=args.eps, patience=args.patience)  # one full replica per rank
+    eps, p = w.eps_mag, w.patience
+    dev = K.DeviceInputs(w)
+    queries = w.batch * w.num_q_heads
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > L2 (126 MB)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def time_calls(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        barrier()
+        for i in range(steps):
+            flush.fill_(i & 255)
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        barrier()
+        return np.array([a.elapsed_time(b) for a, b in evs])  # ms
+
+    art_call = lambda: dev.art(eps, eps, p, stream=stream)
+    dense_call = lambda: dev.dense(stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        art_call()
+    torch.cuda.synchronize()
+    bu = dev.blocks_used.cpu().numpy().reshape(-1).copy()
+    status = dev.status()
+
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    time.sleep(0.3)
+    t_art = time_calls(art_call, args.steps)
+    clocks = clk.stop()
+    ms = float(t_art.mean())
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = ws * queries / (ms * 1e-3)
+
+    # dense twin on the same buffers
+    dense = None
+    if not args.no_dense:
+        for _ in range(max(3, args.warmup)):
+            dense_call()
+        t_d = time_calls(dense_call, args.steps)
+        ms_d = float(t_d.mean())
+        dense = {"queries_per_s": queries / (ms_d * 1e-3), "ms_per_step": ms_d,
+                 "gbs": (kv_bytes(w) + side_bytes(w)) / (ms_d * 1e-3) / 1e9, "speedup_art_over_dense": ms_d / ms}
+        # the detector's own cost: ART with eps = 0 never stops
+        zero = lambda: dev.art(0.0, 0.0, p, stream=stream)
+        for _ in range(3):
+            zero()
+        ms_z = float(time_calls(zero, args.steps).mean())
+        dense["art_eps0_ms_per_step"] = ms_z
+        dense["detector_overhead_frac"] = ms_z / ms_d - 1.0
+
+    # roofline of the decode kernel (bytes actually needed by the blocks processed)
+    peak, peak_kind = load_peaks()
+    alg = kv_bytes(w, bu) + side_bytes(w)
+    achieved = alg / (ms * 1e-3) / 1e9
+    traffic, _ = load_traffic(w.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg,
+                "timed": "whole art_decode call (workspace memset + plan kernel + decode kernel)"}
+
+    # end to end through the public API with host buffers: per step the step's
+    # inputs (queries, lengths, page table, visit lists) go host->device and the
+    # outputs (attention output, blocks_used) come back; the KV cache is the
+    # device-resident state of the serving engine.
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for name in ("q", "seq_lens", "block_table", "visit_order"):
+            t = getattr(dev, name)
+            if t is not None:
+                host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+        out_h = torch.empty(dev.out.shape, dtype=dev.out.dtype, pin_memory=True)
+        bu_h = torch.empty(dev.blocks_used.shape, dtype=torch.int32, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size() + bu_h.numel() * 4
+
+        def e2e_step():
+            for name, t in host.items():
+                getattr(dev, name).copy_(t, non_blocking=True)
+            art_call()
+            out_h.copy_(dev.out, non_blocking=True)
+            bu_h.copy_(dev.blocks_used, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        t_e = time_calls(e2e_step, args.steps)
+        ms_e = float(t_e.mean())
+        e2e = {"value": ws * queries / (ms_e * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e,
+               "note": "KV cache resident on the device; per-step inputs and outputs copied"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, eps, p)
+
+    if rank == 0:
+        n = w.visit_lengths()
+        line = {"metric": "decode-attention queries/s (ART)", "value": value, "unit": "queries/s",
+                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+                "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+                           "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+                           "block_size": w.block_size, "eps": eps, "patience": p,
+                           "l2": "flushed (256 MB write) before every timed call; inputs also exceed L2",
+                           "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+                "gpu_launches": 2 * args.steps,
+                "dense_twin": dense,
+                "blocks_used": {"mean": float(bu.mean()), "listed_mean": float(n.mean()),
+                                "fraction": float(bu.sum() / max(1, n.sum()))},
+                "status": status}
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+// art_common.cuh -- shared definitions of the ART decode-attention kernels:
+// launch parameters, workspace layout, and thin wrappers around the sm_100+
+// PTX used for the shared-memory ring (mbarrier, cp.async.bulk).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "art.h"
+
+namespace art {
+
+constexpr int kBK = 64;          // tokens per ART block (the unit of the stability test)
+constexpr int kNWC = 4;          // consumer warps per CTA
+constexpr int kMaxProbe = 32;    // probe entries per query head
+constexpr int kThreads = (kNWC + 2) * 32;  // consumers, then the producer warp, then the statistics warp
+constexpr int kProducerWarp = kNWC;
+constexpr int kStatWarp = kNWC + 1;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
+
+// Item flags written by the plan kernel.
+constexpr int kItemHas0 = 1;     // logical block 0 is in the visit list
+constexpr int kItemBad = 2;      // the item's device data failed a check
+
+// Slot kinds written by the producer into the ring metadata.
+enum SlotKind : int { kSlotBlock = 0, kSlotEmpty = 1, kSlotFail = 2, kSlotEnd = 3 };
+
+struct WsHeader {
+    unsigned int claim;      // next position of `order` to hand out
+    unsigned int plan_done;  // plan CTAs that have finished
+    int status;              // ART_STATUS_* bits
+    int pad[13];
+};
+static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
+
+struct ItemInfo {
+    int n;      // listed blocks
+    int flags;  // kItemHas0 | kItemBad
+};
+
+struct Params {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* visit;  // may be null (natural order)
+    const int32_t* probe;  // may be null for the dense twin
+    void* out;
+    int32_t* blocks_used;  // may be null for the dense twin
+    WsHeader* hdr;
+    const int32_t* order;
+    const ItemInfo* info;
+    int B, Hq, Hkv, Ps, max_pages, max_visit, m, num_pages, num_items, stages;
+    float eps_mag, eps_dir;
+    int patience;
+};
+
+// Launch geometry chosen for one call.
+struct LaunchInfo {
+    int grid;
+    int stages;
+    size_t smem;
+    int ctas_per_sm;
+};
+
+// Workspace: header, then ItemInfo[num_items], then the claim order int32[num_items].
+inline size_t workspace_bytes_for(int num_items) {
+    return sizeof(WsHeader) + (size_t)num_items * (sizeof(int32_t) + sizeof(ItemInfo));
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bulk copy global -> this CTA's shared memory, completing on `bar` (tx bytes).
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ int ld_volatile_shared(const int* p) { return *(const volatile int*)p; }
+__device__ __forceinline__ void st_volatile_shared(int* p, int v) { *(volatile int*)p = v; }
+
+// ---------------------------------------------------------------------------
+// element unpacking: 16 bytes of the row chunk -> EPC floats
+// ---------------------------------------------------------------------------
+template <bool kBF16>
+struct Elem;
+
+template <>
+struct Elem<true> {
+    static constexpr int kEPC = 8;
+    static constexpr int kBytes = 2;
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        f[0] = __uint_as_float(u.x << 16);
+        f[1] = __uint_as_float(u.x & 0xffff0000u);
+        f[2] = __uint_as_float(u.y << 16);
+        f[3] = __uint_as_float(u.y & 0xffff0000u);
+        f[4] = __uint_as_float(u.z << 16);
+        f[5] = __uint_as_float(u.z & 0xffff0000u);
+        f[6] = __uint_as_float(u.w << 16);
+        f[7] = __uint_as_float(u.w & 0xffff0000u);
+    }
+    // round to nearest even
+    __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
+        uint32_t u = __float_as_uint(x);
+        uint32_t r = (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+        if ((u & 0x7fffffffu) > 0x7f800000u) r = 0x7fc0u;  // NaN stays NaN
+        static_cast<uint16_t*>(base)[idx] = static_cast<uint16_t>(r);
+    }
+};
+
+template <>
+struct Elem<false> {
+    static constexpr int kEPC = 4;
+    static constexpr int kBytes = 4;
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
+        static_cast<float*>(base)[idx] = x;
+    }
+};
+
+}  // namespace art

@@ -1,0 +1,112 @@
+"""The C-ABI library loads, exports every function include/art.h declares, and
+rejects bad arguments on the host (no GPU, no compute call). CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kv_cache_early_gb300 as K
+from kv_cache_early_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "art.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return K.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("art_decode", "dense_decode", "art_workspace_bytes", "art_read_device_status", "art_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in art.h but not exported"
+        assert getattr(lib, n) is not None
+
+
+def test_shape_struct_matches_header():
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct art_shape \{(.*?)\} art_shape;", src, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"int32_t\s+(\w+);", body)
+    assert fields == [f[0] for f in K.ArtShape._fields_]
+    assert ctypes.sizeof(K.ArtShape) == 4 * len(fields)
+
+
+def good_shape(**kw):
+    s = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, block_size=64,
+             max_pages_per_seq=8, max_visit=2, num_probe=32, num_pages_total=16, dtype=0)
+    s.update(kw)
+    return K.make_shape(**s)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case below fails a host check first
+
+
+def call_art(lib, shape, q=FAKE, probe=FAKE, bu=FAKE, ws=FAKE, ws_bytes=1 << 20, patience=2, em=1e-3, ed=1e-3):
+    P = ctypes.c_void_p
+    return lib.art_decode(P(q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, em, ed, patience, P(probe), P(FAKE),
+                          P(bu), None if shape is None else ctypes.byref(shape), P(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(shape=None), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(num_q_heads=7, num_kv_heads=2)), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(num_q_heads=6, num_kv_heads=2)), K.ART_ERR_UNSUPPORTED),  # G = 3
+    (dict(shape=good_shape(head_dim=96)), K.ART_ERR_UNSUPPORTED),
+    (dict(shape=good_shape(block_size=32)), K.ART_ERR_UNSUPPORTED),
+    (dict(shape=good_shape(page_size=12)), K.ART_ERR_UNSUPPORTED),
+    (dict(shape=good_shape(page_size=4)), K.ART_ERR_UNSUPPORTED),
+    (dict(shape=good_shape(dtype=5)), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(batch=0)), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(num_probe=33)), K.ART_ERR_UNSUPPORTED),
+    (dict(shape=good_shape(num_probe=0)), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), patience=0), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), em=float("nan")), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), ed=-1.0), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), q=0), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), q=FAKE + 4), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), probe=0), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), bu=0), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), ws=FAKE + 8), K.ART_ERR_INVALID_ARG),
+    (dict(shape=good_shape(), ws_bytes=16), K.ART_ERR_WORKSPACE),
+])
+def test_host_argument_checks(lib, case, expect):
+    assert call_art(lib, **case) == expect
+
+
+def test_dense_host_checks(lib):
+    P = ctypes.c_void_p
+    s = good_shape()
+    assert lib.dense_decode(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), ctypes.byref(s), P(FAKE),
+                            8, None) == K.ART_ERR_WORKSPACE
+    assert lib.dense_decode(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), ctypes.byref(s), P(FAKE),
+                            1 << 20, None) == K.ART_ERR_INVALID_ARG
+    # the dense twin ignores the probe and the thresholds
+    s2 = good_shape(num_probe=0)
+    assert lib.dense_decode(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), ctypes.byref(s2), P(FAKE),
+                            8, None) == K.ART_ERR_WORKSPACE
+
+
+def test_workspace_size(lib):
+    s = good_shape(batch=3, num_kv_heads=4, num_q_heads=16)
+    assert K.art_workspace_bytes(s) == 64 + 12 * 12
+    assert lib.art_workspace_bytes(None) == 0
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, 7):
+        assert lib.art_status_string(code)
