@@ -58,6 +58,19 @@ def dist_info():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over the ranks of the default process group
+    (x itself without one). Used for the step time: the job is as slow as its
+    slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------
 # byte accounting (algorithmic bytes of one call)
 # ---------------------------------------------------------------------------
@@ -296,12 +309,7 @@ def run_ours(args):
     time.sleep(0.3)
     t_art = time_calls(art_call, args.steps)
     clocks = clk.stop()
-    ms = float(t_art.mean())
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(t_art.mean()), device="cuda")
     value = ws * queries / (ms * 1e-3)
 
     # dense twin on the same buffers

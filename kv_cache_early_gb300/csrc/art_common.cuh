@@ -11,7 +11,7 @@
 namespace art {
 
 constexpr int kBK = 64;          // tokens per ART block (the unit of the stability test)
-constexpr int kNWC = 4;          // consumer warps per CTA
+constexpr int kNWC = 8;          // consumer warps per CTA
 constexpr int kMaxProbe = 32;    // probe entries per query head
 constexpr int kThreads = (kNWC + 2) * 32;  // consumers, then the producer warp, then the statistics warp
 constexpr int kProducerWarp = kNWC;
@@ -121,28 +121,57 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Named barrier among the consumer warps only (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic; each half is an IEEE fp32 op).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void up2(uint64_t r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ int ld_volatile_shared(const int* p) { return *(const volatile int*)p; }
 __device__ __forceinline__ void st_volatile_shared(int* p, int v) { *(volatile int*)p = v; }
 
 // ---------------------------------------------------------------------------
-// element unpacking: 16 bytes of the row chunk -> EPC floats
+// element handling. A lane reads CB bytes (one "chunk") of a K/V/q row and
+// turns them into packed fp32 pairs (elements 2i, 2i+1 of the chunk).
 // ---------------------------------------------------------------------------
 template <bool kBF16>
 struct Elem;
 
 template <>
 struct Elem<true> {
-    static constexpr int kEPC = 8;
     static constexpr int kBytes = 2;
-    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
-        f[0] = __uint_as_float(u.x << 16);
-        f[1] = __uint_as_float(u.x & 0xffff0000u);
-        f[2] = __uint_as_float(u.y << 16);
-        f[3] = __uint_as_float(u.y & 0xffff0000u);
-        f[4] = __uint_as_float(u.z << 16);
-        f[5] = __uint_as_float(u.z & 0xffff0000u);
-        f[6] = __uint_as_float(u.w << 16);
-        f[7] = __uint_as_float(u.w & 0xffff0000u);
+    template <int CB>
+    __device__ __forceinline__ static void load_pairs(const unsigned char* src, uint64_t* f2) {
+        if constexpr (CB == 8) {
+            const uint2 u = *reinterpret_cast<const uint2*>(src);
+            f2[0] = pk2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+            f2[1] = pk2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+        } else {
+            const uint4 u = *reinterpret_cast<const uint4*>(src);
+            f2[0] = pk2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+            f2[1] = pk2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+            f2[2] = pk2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
+            f2[3] = pk2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+        }
     }
     // round to nearest even
     __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
@@ -155,13 +184,17 @@ struct Elem<true> {
 
 template <>
 struct Elem<false> {
-    static constexpr int kEPC = 4;
     static constexpr int kBytes = 4;
-    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
-        f[0] = __uint_as_float(u.x);
-        f[1] = __uint_as_float(u.y);
-        f[2] = __uint_as_float(u.z);
-        f[3] = __uint_as_float(u.w);
+    template <int CB>
+    __device__ __forceinline__ static void load_pairs(const unsigned char* src, uint64_t* f2) {
+        if constexpr (CB == 8) {
+            const uint2 u = *reinterpret_cast<const uint2*>(src);
+            f2[0] = pk2(__uint_as_float(u.x), __uint_as_float(u.y));
+        } else {
+            const uint4 u = *reinterpret_cast<const uint4*>(src);
+            f2[0] = pk2(__uint_as_float(u.x), __uint_as_float(u.y));
+            f2[1] = pk2(__uint_as_float(u.z), __uint_as_float(u.w));
+        }
     }
     __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
         static_cast<float*>(base)[idx] = x;

@@ -1,36 +1,43 @@
 // art_kernel.cuh -- the persistent, warp-specialized ART decode-attention kernel.
 //
 // One CTA runs three roles over a ring of `stages` shared-memory slots, each
-// slot holding one ART block of K rows, V rows and (for an item's first
-// block) the item's G query vectors:
+// slot holding one 64-token ART block of K rows, V rows and (for an item's
+// first block) the item's G query vectors:
 //
-//   producer warp   claims work items (sequence b, KV head g) in the order
-//                   the plan kernel wrote (longest visit list first), resolves
+//   producer warp   claims work items (sequence b, KV head g) in the order the
+//                   plan kernel wrote (longest visit list first), resolves
 //                   visit entry -> logical block -> physical pages through the
 //                   block table, and fills slots with cp.async.bulk copies that
 //                   complete on the slot's mbarrier. It stops issuing an item's
-//                   blocks as soon as the statistics warp has stopped that item.
-//   consumer warps  (kNWC) each own 16 of the block's 64 rows: scores
-//                   s = q.k * log2(e)/sqrt(d) in fp32, a block-local softmax
-//                   (max m_w, weights p = 2^(s - m_w), sum l_w), the block's
-//                   P.V partial, then an online-softmax fold into per-warp
-//                   running accumulators (ART paper sec. 3.1: FlashAttention's
-//                   streaming softmax; O^(t) after t blocks).
-//   statistics warp merges the consumer warps' (m_w, l_w, P.V at the probe
-//                   columns) in visit order into the probe x^(i) of O^(i), and
+//                   blocks once the statistics warp has stopped that item.
+//   consumer warps  (kNWC) each own 8 of the block's 64 rows. Scores
+//                   s = q.k * log2(e)/sqrt(d) in fp32; the block's largest
+//                   score per head is shared through a named barrier; weights
+//                   p = 2^(s - m_blk); the block's P.V partial; and an online-
+//                   softmax fold into the running accumulators (ART paper
+//                   sec. 3.1: FlashAttention's streaming softmax, O^(t) after
+//                   t blocks). Arithmetic on packed fp32 pairs (f32x2).
+//   statistics warp merges the consumer warps' block sums and P.V at the probe
+//                   columns, in visit order, into the probe x^(i) of O^(i), and
 //                   evaluates the stability test (magnitude and direction
-//                   change, both below their thresholds, for `patience`
-//                   consecutive blocks, never before block 0) -- ART paper
-//                   sec. 3.2 and the gist.science explainer sec. 2.2-2.4.
+//                   change both below their thresholds for `patience`
+//                   consecutive blocks, never before block 0 has been
+//                   processed) -- ART paper sec. 3.2, gist.science explainer
+//                   sec. 2.2-2.4.
+//
+// The consumers do not wait for the decision on block i before computing
+// block i+1 (G <= 4): block i+1 is held apart and folded only once block i's
+// decision says "continue"; after a stop it is discarded. For G > 4 (register
+// budget) each block waits for its own decision.
 //
 // The statistics avoid cancellation: the change of the probe over block i is
 // formed directly, delta = b (P.V_probe - l_blk x^(i-1)) / L_i, the norm
 // change as delta.(2x + delta) / (|x_i| + |x_{i-1}|), and 1 - cos as
 // |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2.
 //
-// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets
-// ART_STATUS_TIMEOUT, lets the producer wait for its own copies in flight,
-// and returns.
+// Every mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel sets
+// ART_STATUS_TIMEOUT, the producer waits for its own copies in flight, and
+// the CTA returns.
 #pragma once
 
 #include "art_common.cuh"
@@ -45,14 +52,19 @@ __host__ __device__ constexpr int pow2ceil(int x) {
 __host__ __device__ constexpr int imax(int a, int b) { return a > b ? a : b; }
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+enum Decision : int { kContinue = 0, kStop = 1, kDiscard = 2 };
+
 template <bool kBF16, int D, int G>
 struct Cfg {
     using E = Elem<kBF16>;
     static constexpr int GQ = G;                 // query heads per KV head
-    static constexpr int EPC = E::kEPC;          // elements per 16-byte chunk
     static constexpr int ELT = E::kBytes;
+    static constexpr int DD = D;
     static constexpr int ROWB = D * ELT;         // bytes of one K or V row
-    static constexpr int LPR = ROWB / 16;        // lanes covering one row
+    static constexpr int CB = ROWB / 8 <= 32 ? 8 : 16;  // bytes of a row one lane reads
+    static constexpr int EPC = CB / ELT;         // elements per chunk
+    static constexpr int E2 = EPC / 2;           // packed pairs per chunk
+    static constexpr int LPR = ROWB / CB;        // lanes covering one row
     static constexpr int RPW = 32 / LPR;         // rows per warp instruction
     static constexpr int RW = kBK / kNWC;        // rows per consumer warp per block
     static constexpr int NI = RW / RPW;          // warp instructions per block
@@ -62,12 +74,11 @@ struct Cfg {
     static constexpr int KVB = kBK * ROWB;       // bytes of K (or V) of one block
     static constexpr int SLOT = 2 * KVB + QB;
     static constexpr int SPL = (G * kMaxProbe + 31) / 32;  // probe slots per stat lane
-    static constexpr int PART_F = 2 * kNWC * RPW * G * kMaxProbe;  // probe partial floats
-    static constexpr int WACC_F = kNWC * G * D;                     // epilogue floats
-    static constexpr int UNION_F = imax(PART_F, WACC_F);
-    static_assert(LPR >= 8 && LPR <= 32, "row must be 128..512 bytes");
-    static_assert(RW % RPW == 0, "rows per warp");
-    static_assert(RW == 16, "softmax groups assume 16 rows per warp");
+    static constexpr int PART_F = 2 * kNWC * RPW * G * kMaxProbe;
+    static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
+    static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
+    static_assert(RW % RPW == 0 && NI >= 1, "rows per warp");
+    static_assert(32 % RW == 0, "softmax lane groups");
     static_assert(G >= 1 && G <= 8, "group size");
 };
 
@@ -83,11 +94,12 @@ struct Ctrl {
 };
 
 struct Layout {
-    size_t meta, bars, part, pmeta, scr, wml, ptab, ctrl, total;
+    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, sh, ptab, ctrl, total;
 };
 
 template <class C>
 __host__ __device__ inline Layout make_layout(int stages) {
+    constexpr int G = C::GQ;
     Layout L;
     size_t o = (size_t)stages * C::SLOT;
     L.meta = o;
@@ -96,14 +108,22 @@ __host__ __device__ inline Layout make_layout(int stages) {
     L.bars = o;
     o += (size_t)(2 * stages + 5) * sizeof(uint64_t);
     o = align_up(o, 16);
-    L.part = o;
-    o += (size_t)C::UNION_F * sizeof(float);
-    L.pmeta = o;
-    o += (size_t)2 * kNWC * 2 * C::GQ * sizeof(float);
-    L.scr = o;
-    o += (size_t)kNWC * (C::GQ * C::RW + 2 * C::GQ) * sizeof(float);
-    L.wml = o;
-    o += (size_t)kNWC * 2 * C::GQ * sizeof(float);
+    L.part = o;  // [2][NWC][RPW][G][kMaxProbe] probe partials
+    o += (size_t)C::PART_F * sizeof(float);
+    L.plb = o;  // [2][NWC][G] per-warp block sums
+    o += (size_t)2 * kNWC * G * sizeof(float);
+    L.pmb = o;  // [2][G] block maxima
+    o += (size_t)2 * G * sizeof(float);
+    L.wmax = o;  // [NWC][G] per-warp maxima of the block being processed
+    o += (size_t)kNWC * G * sizeof(float);
+    L.scr = o;  // [NWC][G][RW] scores, then weights
+    o += (size_t)kNWC * G * C::RW * sizeof(float);
+    o = align_up(o, 16);
+    L.eacc = o;  // per consumer warp: [G][D] output sums, then [G] weight sums
+    o += (size_t)kNWC * (G * C::DD + G) * sizeof(float);
+    o = align_up(o, 16);
+    L.sh = o;  // [3][G] statistics warp scratch
+    o += (size_t)3 * G * sizeof(float);
     o = align_up(o, 16);
     L.ptab = o;
     o += (size_t)2 * C::LPR * sizeof(int);
@@ -330,20 +350,30 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
 // statistics warp (ART only)
 // ---------------------------------------------------------------------------
 template <class C>
-__device__ void stat_warp(const Params& p, const float* part, const float* pmeta, uint64_t* part_full,
-                          uint64_t* dec_bar, Ctrl* ctrl) {
+__device__ void stat_warp(const Params& p, const float* part, const float* plb, const float* pmb, float* sh,
+                          uint64_t* part_full, uint64_t* dec_bar, Ctrl* ctrl) {
     constexpr int G = C::GQ;
     constexpr int SPL = C::SPL;
+    constexpr int RPW = C::RPW;
     const int lane = threadIdx.x & 31;
     const int m = p.m;
     const int GM = G * m;
-    float M[G], Lsum[G];
+    // the probe slot of each (lane, j): head and column rank
+    int hs[SPL], ss[SPL];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) {
+        const int k = lane + 32 * j;
+        hs[j] = k < GM ? k / m : -1;
+        ss[j] = k < GM ? k - (k / m) * m : 0;
+    }
+    float Mh = -INFINITY, Lh = 0.f;  // running max / sum of head `lane` (lanes < G)
     float X[SPL], dl[SPL];
     float nprev = 0.f;
     int counter = 0, seen0 = 0;
+    int stopped_item = -1;
     auto reset = [&]() {
-#pragma unroll
-        for (int h = 0; h < G; ++h) { M[h] = -INFINITY; Lsum[h] = 0.f; }
+        Mh = -INFINITY;
+        Lh = 0.f;
 #pragma unroll
         for (int j = 0; j < SPL; ++j) X[j] = 0.f;
         nprev = 0.f;
@@ -356,61 +386,42 @@ __device__ void stat_warp(const Params& p, const float* part, const float* pmeta
         if (!wait_bounded(&part_full[vb], (uint32_t)(v >> 1) & 1u, ctrl, p.hdr)) return;
         const SlotMeta info = ctrl->info[vb];
         if (info.kind == kSlotEnd) return;
-        int stop = 1;
-        if (info.kind == kSlotBlock) {
+        int dec = kStop;
+        if (info.kind != kSlotBlock) {
+            if (lane == 0) p.blocks_used[info.item] = info.kind == kSlotFail ? -1 : 0;
+            reset();
+        } else if (info.item == stopped_item) {
+            dec = kDiscard;  // computed ahead of the decision that stopped its item
+        } else {
             if (info.pos == 0) reset();
-            // merge the consumer warps' block partials: common block max, weights
-            float mb[G], lb[G], ew[kNWC][G];
-            const float* pm = pmeta + (size_t)vb * kNWC * 2 * G;
+            // per head: block sum over the warps, new running max and sum
+            if (lane < G) {
+                const float mb = pmb[vb * G + lane];
+                float lb = 0.f;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kNWC; ++w) mx = fmaxf(mx, pm[w * 2 * G + h]);
-                float l = 0.f;
-#pragma unroll
-                for (int w = 0; w < kNWC; ++w) {
-                    const float mw = pm[w * 2 * G + h];
-                    ew[w][h] = mw == -INFINITY ? 0.f : exp2f(mw - mx);
-                    l += ew[w][h] * pm[w * 2 * G + G + h];
-                }
-                mb[h] = mx;
-                lb[h] = l;
+                for (int w = 0; w < kNWC; ++w) lb += plb[(vb * kNWC + w) * G + lane];
+                const float Mn = fmaxf(Mh, mb);
+                const float a = exp2f(Mh - Mn);
+                const float bw = exp2f(mb - Mn);
+                const float Ln = a * Lh + bw * lb;
+                sh[lane] = bw;
+                sh[G + lane] = lb;
+                sh[2 * G + lane] = Ln;
+                Mh = Mn;
+                Lh = Ln;
             }
-            float Mn[G], Ln[G], bw[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                Mn[h] = fmaxf(M[h], mb[h]);
-                const float a = exp2f(M[h] - Mn[h]);
-                bw[h] = exp2f(mb[h] - Mn[h]);
-                Ln[h] = a * Lsum[h] + bw[h] * lb[h];
-            }
-            const float* pp = part + (size_t)vb * kNWC * C::RPW * G * kMaxProbe;
+            __syncwarp();
+            const float* pp = part + (size_t)vb * kNWC * RPW * G * kMaxProbe;
             float sx2 = 0.f, sdd = 0.f;
 #pragma unroll
             for (int j = 0; j < SPL; ++j) {
-                const int k = lane + 32 * j;
                 dl[j] = 0.f;
-                if (k < GM) {
-                    const int h = k / m, s = k - (k / m) * m;
+                const int h = hs[j];
+                if (h >= 0) {
                     float pb = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kNWC; ++w) {
-                        float t = 0.f;
-#pragma unroll
-                        for (int hf = 0; hf < C::RPW; ++hf)
-                            t += pp[((w * C::RPW + hf) * G + h) * kMaxProbe + s];
-                        float e = 0.f;
-#pragma unroll
-                        for (int hh = 0; hh < G; ++hh)
-                            if (hh == h) e = ew[w][hh];
-                        pb += e * t;
-                    }
-                    float hb = 0.f, hl = 0.f, hL = 1.f;
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-                        if (hh == h) { hb = bw[hh]; hl = lb[hh]; hL = Ln[hh]; }
-                    const float d = hb * (pb - hl * X[j]) / hL;
+                    for (int w = 0; w < kNWC * RPW; ++w) pb += pp[(w * G + h) * kMaxProbe + ss[j]];
+                    const float d = sh[h] * (pb - sh[G + h] * X[j]) / sh[2 * G + h];
                     dl[j] = d;
                     const float x = X[j] + d;
                     sx2 += x * x;
@@ -427,8 +438,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* pmeta
                 const float cx = dn / (ni * nprev);
 #pragma unroll
                 for (int j = 0; j < SPL; ++j) {
-                    const int k = lane + 32 * j;
-                    if (k < GM) {
+                    if (hs[j] >= 0) {
                         const float u = dl[j] / ni - X[j] * cx;
                         su2 += u * u;
                     }
@@ -441,22 +451,22 @@ __device__ void stat_warp(const Params& p, const float* part, const float* pmeta
             }
             counter = stable ? counter + 1 : 0;
             if (info.c == 0) seen0 = 1;
-            stop = ((counter >= p.patience) && (seen0 || !info.has0)) || (info.pos == info.n - 1);
+            const bool stop = ((counter >= p.patience) && (seen0 || !info.has0)) || (info.pos == info.n - 1);
 #pragma unroll
             for (int j = 0; j < SPL; ++j) X[j] += dl[j];
-#pragma unroll
-            for (int h = 0; h < G; ++h) { M[h] = Mn[h]; Lsum[h] = Ln[h]; }
             nprev = ni;
-            if (stop && lane == 0) {
-                p.blocks_used[info.item] = info.pos + 1;
-                st_volatile_shared(&ctrl->stop_item, info.item);
+            dec = stop ? kStop : kContinue;
+            if (stop) {
+                stopped_item = info.item;
+                if (lane == 0) {
+                    p.blocks_used[info.item] = info.pos + 1;
+                    st_volatile_shared(&ctrl->stop_item, info.item);
+                }
             }
-        } else {
-            if (lane == 0) p.blocks_used[info.item] = info.kind == kSlotFail ? -1 : 0;
-            reset();
         }
+        __syncwarp();
         if (lane == 0) {
-            ctrl->dec[vb] = stop;
+            ctrl->dec[vb] = dec;
             mbar_arrive(&dec_bar[vb]);
         }
         __syncwarp();
@@ -469,41 +479,58 @@ __device__ void stat_warp(const Params& p, const float* part, const float* pmeta
 template <class C, bool kART>
 __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotMeta* meta, uint64_t* full,
                                uint64_t* empty, uint64_t* part_full, uint64_t* dec_bar, uint64_t* cbar,
-                               float* part, float* pmeta, float* scr_all, float* wml, const int* pmask,
-                               const int* pbase, Ctrl* ctrl) {
+                               const Layout& L, unsigned char* smem, const int* pmask, const int* pbase,
+                               Ctrl* ctrl) {
     constexpr int G = C::GQ;
-    constexpr int EPC = C::EPC, LPR = C::LPR, RPW = C::RPW, RW = C::RW, NI = C::NI;
-    constexpr int D = C::ROWB / C::ELT;
+    constexpr int EPC = C::EPC, E2 = C::E2, LPR = C::LPR, RPW = C::RPW, RW = C::RW, NI = C::NI;
+    constexpr int D = C::DD;
+    constexpr bool LAG = kART && C::LAG;
     using E = typename C::E;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane / LPR, ch = lane % LPR;
-    float* scr = scr_all + (size_t)w * (G * RW + 2 * G);  // [G][RW] scores / weights, then m_w[G], l_w[G]
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    float* plb = reinterpret_cast<float*>(smem + L.plb);
+    float* pmb = reinterpret_cast<float*>(smem + L.pmb);
+    float* wmax = reinterpret_cast<float*>(smem + L.wmax);
+    float* scr = reinterpret_cast<float*>(smem + L.scr) + (size_t)w * G * RW;  // [G][RW]
+    float* eacc = reinterpret_cast<float*>(smem + L.eacc);                   // [NWC][G*D + G]
     const float qscale = 1.4426950408889634f / sqrtf((float)D);
     const uint32_t my_mask = (uint32_t)pmask[ch];
     const int my_base = pbase[ch];
+    const int ctid = threadIdx.x;  // 0 .. kNWC*32-1
 
-    float qs[G][EPC], acc[G][EPC], mrun[G], lrun[G];
+    uint64_t qs[G][E2];    // pre-scaled queries of this lane's chunk
+    uint64_t acc[G][E2];   // running P.V of this lane's rows (scale m_run)
+    uint64_t tN[G][E2];    // block just computed
+    uint64_t tP[G][E2];    // block waiting for its decision (LAG)
+    float mrun[G], lrun[G], mbN[G], lbN[G], mbP[G], lbP[G];
+    SlotMeta mP;
+    mP.item = -1; mP.b = 0; mP.g = 0;
+    int vP = 0;
+    bool pending = false;
+
     auto reset = [&]() {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             mrun[h] = -INFINITY;
             lrun[h] = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) acc[h][e] = 0.f;
+            for (int e = 0; e < E2; ++e) acc[h][e] = 0ull;
         }
     };
     reset();
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < G; ++h) {
+        mbN[h] = mbP[h] = lbN[h] = lbP[h] = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) qs[h][e] = 0.f;
+        for (int e = 0; e < E2; ++e) { qs[h][e] = 0ull; tN[h][e] = 0ull; tP[h][e] = 0ull; }
+    }
 
     int slot = 0;
     uint32_t round = 0;
-    int v = 0;          // partials published (ART)
+    int v = 0;          // records published to the statistics warp
     uint32_t cbph = 0;  // consumer-barrier phase
     int stopped_item = -1;
-    const int ctid = threadIdx.x;  // 0 .. kNWC*32-1
 
     auto cbar_sync = [&]() -> bool {
         __syncwarp();
@@ -519,41 +546,106 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     auto advance = [&]() {
         if (++slot == p.stages) { slot = 0; ++round; }
     };
-    auto out_ptr_index = [&](int b, int g, int h, int col) -> size_t {
+    auto out_index = [&](int b, int g, int h, int col) -> size_t {
         return ((size_t)b * p.Hq + (size_t)g * G + h) * D + col;
     };
-    auto write_zero = [&](int b, int g) {
-        for (int idx = ctid; idx < G * D; idx += kNWC * 32) E::store(p.out, out_ptr_index(b, g, idx / D, idx % D), 0.f);
-    };
-    // publish a record for the statistics warp and wait for its decision
-    auto publish_and_decide = [&](const SlotMeta& mt) -> int {
+    auto publish = [&](const SlotMeta& mt) -> int {  // returns the record number
         const int vb = v & 1;
         if (w == 0 && lane == 0) ctrl->info[vb] = mt;
         __syncwarp();
         if (lane == 0) mbar_arrive(&part_full[vb]);
-        const bool okw = wait_bounded(&dec_bar[vb], (uint32_t)(v >> 1) & 1u, ctrl, p.hdr);
-        ++v;
-        if (!okw) return -1;
-        return ctrl->dec[vb];
+        return v++;
+    };
+    auto wait_dec = [&](int rec) -> int {
+        if (!wait_bounded(&dec_bar[rec & 1], (uint32_t)(rec >> 1) & 1u, ctrl, p.hdr)) return -1;
+        return ctrl->dec[rec & 1];
+    };
+    auto fold = [&](const uint64_t (&t)[G][E2], const float* mb, const float* lb) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float mn = fmaxf(mrun[h], mb[h]);
+            const float a = exp2f(mrun[h] - mn);
+            const float bb = exp2f(mb[h] - mn);
+            const uint64_t a2 = pk2(a, a), b2 = pk2(bb, bb);
+#pragma unroll
+            for (int e = 0; e < E2; ++e) acc[h][e] = fma2(b2, t[h][e], mul2(a2, acc[h][e]));
+            lrun[h] = a * lrun[h] + bb * lb[h];
+            mrun[h] = mn;
+        }
+    };
+    // all warps share the block maxima, so the running maxima agree across warps;
+    // the warps' partial sums are added in a fixed order (reproducible results)
+    auto epilogue = [&](int b, int g) -> bool {
+        float fa[G][EPC];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < E2; ++e) up2(acc[h][e], fa[h][2 * e], fa[h][2 * e + 1]);
+#pragma unroll
+        for (int s = LPR; s < 32; s <<= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) fa[h][e] += __shfl_xor_sync(0xffffffffu, fa[h][e], s);
+        float* mine = eacc + (size_t)w * (G * D + G);  // this warp's [G][D] sums, then [G] weights
+        if (half == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) mine[h * D + ch * EPC + e] = fa[h][e];
+        }
+        if (lane < G) {
+            float l = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                if (h == lane) l = lrun[h];
+            mine[G * D + lane] = l;
+        }
+        if (!cbar_sync()) return false;
+        for (int idx = ctid; idx < G * D; idx += kNWC * 32) {
+            const int h = idx / D, col = idx - (idx / D) * D;
+            float num = 0.f, den = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kNWC; ++ww) {
+                num += eacc[(size_t)ww * (G * D + G) + idx];
+                den += eacc[(size_t)ww * (G * D + G) + G * D + h];
+            }
+            E::store(p.out, out_index(b, g, h, col), num / den);
+        }
+        return cbar_sync();  // eacc is free again
+    };
+    auto write_zero = [&](int b, int g) {
+        for (int idx = ctid; idx < G * D; idx += kNWC * 32)
+            E::store(p.out, out_index(b, g, idx / D, idx % D), 0.f);
+    };
+    // resolves the pending block; returns false on abort
+    auto resolve_pending = [&]() -> bool {
+        const int d = wait_dec(vP);
+        if (d < 0) return false;
+        fold(tP, mbP, lbP);
+        pending = false;
+        if (d == kStop) {
+            if (!epilogue(mP.b, mP.g)) return false;
+            reset();
+            stopped_item = mP.item;
+        }
+        return true;
     };
 
     for (;;) {
         if (!wait_bounded(&full[slot], round & 1u, ctrl, p.hdr)) return;
         const SlotMeta mt = meta[slot];
         if (mt.kind == kSlotEnd) {
-            if (kART) {
-                const int vb = v & 1;
-                if (w == 0 && lane == 0) ctrl->info[vb] = mt;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&part_full[vb]);
-            }
+            if (LAG && pending && !resolve_pending()) return;
+            if (kART) publish(mt);
             return;
         }
         if (mt.kind != kSlotBlock) {
             release();
+            if (LAG && pending && !resolve_pending()) return;
             if (mt.item != stopped_item) {
                 write_zero(mt.b, mt.g);
-                if (kART && publish_and_decide(mt) < 0) return;
+                if (kART && wait_dec(publish(mt)) < 0) return;
                 reset();
                 stopped_item = mt.item;
             }
@@ -569,18 +661,18 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
         const unsigned char* sV = sK + C::KVB;
         if (mt.pos == 0) {
             const unsigned char* sQ = sK + 2 * C::KVB;
+            const uint64_t sc2 = pk2(qscale, qscale);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const uint4 u = *reinterpret_cast<const uint4*>(sQ + (size_t)h * C::ROWB + ch * 16);
-                float f[EPC];
-                E::unpack(u, f);
+                uint64_t q2[E2];
+                E::template load_pairs<C::CB>(sQ + (size_t)h * C::ROWB + ch * C::CB, q2);
 #pragma unroll
-                for (int e = 0; e < EPC; ++e) qs[h][e] = f[e] * qscale;
+                for (int e = 0; e < E2; ++e) qs[h][e] = mul2(q2[e], sc2);
             }
         }
         const int nvalid = mt.nvalid;
 
-        // ---- scores: partial dots over this lane's chunk, then a transposed reduction
+        // ---- scores of this warp's rows: packed partial dots, transposed reduction
         float sv[C::NVP];
 #pragma unroll
         for (int i = 0; i < C::NVP; ++i) sv[i] = 0.f;
@@ -588,15 +680,16 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
         for (int i = 0; i < NI; ++i) {
             const int r = w * RW + i * RPW + half;
             if (r < nvalid) {
-                const uint4 u = *reinterpret_cast<const uint4*>(sK + (size_t)r * C::ROWB + ch * 16);
-                float kf[EPC];
-                E::unpack(u, kf);
+                uint64_t k2[E2];
+                E::template load_pairs<C::CB>(sK + (size_t)r * C::ROWB + ch * C::CB, k2);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float d = 0.f;
+                    uint64_t d2 = 0ull;
 #pragma unroll
-                    for (int e = 0; e < EPC; ++e) d = fmaf(qs[h][e], kf[e], d);
-                    sv[i * G + h] = d;
+                    for (int e = 0; e < E2; ++e) d2 = fma2(qs[h][e], k2[e], d2);
+                    float lo, hi;
+                    up2(d2, lo, hi);
+                    sv[i * G + h] = lo + hi;
                 }
             }
         }
@@ -613,58 +706,74 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
         }
         __syncwarp();
 
-        // ---- block-local softmax per head over this warp's 16 rows
-        float* wmb = scr + G * RW;
-        float* wlb = wmb + G;
+        // ---- block max per head: this warp's rows, then across warps
 #pragma unroll
         for (int k = 0; k < (G * RW + 31) / 32; ++k) {
             const int idx = k * 32 + lane;
             const int h = idx / RW, rl = idx % RW;
-            const float s = h < G ? scr[h * RW + rl] : -INFINITY;
-            float mx = s;
+            float mx = h < G ? scr[h * RW + rl] : -INFINITY;
 #pragma unroll
             for (int o = RW / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float pw = s == -INFINITY ? 0.f : exp2f(s - mx);
+            if (h < G && rl == 0) wmax[w * G + h] = mx;
+        }
+        named_bar_sync(1, kNWC * 32);
+#pragma unroll
+        for (int k = 0; k < (G * kNWC + 31) / 32; ++k) {
+            const int idx = k * 32 + lane;
+            const int h = idx / kNWC, ww = idx % kNWC;
+            float mx = h < G ? wmax[ww * G + h] : -INFINITY;
+#pragma unroll
+            for (int o = kNWC / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+                if (hh / (32 / kNWC) == k) mbN[hh] = __shfl_sync(0xffffffffu, mx, (hh % (32 / kNWC)) * kNWC);
+        }
+        // ---- weights and this warp's block sums
+#pragma unroll
+        for (int k = 0; k < (G * RW + 31) / 32; ++k) {
+            const int idx = k * 32 + lane;
+            const int h = idx / RW, rl = idx % RW;
+            float mbh = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+                if (hh == h) mbh = mbN[hh];
+            const float s = h < G ? scr[h * RW + rl] : -INFINITY;
+            const float pw = s == -INFINITY ? 0.f : exp2f(s - mbh);
             float sum = pw;
 #pragma unroll
             for (int o = RW / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if (h < G) {
-                scr[h * RW + rl] = pw;
-                if (rl == 0) { wmb[h] = mx; wlb[h] = sum; }
-            }
+            if (h < G) scr[h * RW + rl] = pw;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+                if (hh / (32 / RW) == k) lbN[hh] = __shfl_sync(0xffffffffu, sum, (hh % (32 / RW)) * RW);
         }
         __syncwarp();
-        float mbw[G], lbw[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) { mbw[h] = wmb[h]; lbw[h] = wlb[h]; }
 
-        // ---- P.V for this warp's rows
-        float tmp[G][EPC];
+        // ---- P.V of this warp's rows
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) tmp[h][e] = 0.f;
+            for (int e = 0; e < E2; ++e) tN[h][e] = 0ull;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             const int rl = i * RPW + half;
             const int r = w * RW + rl;
             if (r < nvalid) {
-                const uint4 u = *reinterpret_cast<const uint4*>(sV + (size_t)r * C::ROWB + ch * 16);
-                float vf[EPC];
-                E::unpack(u, vf);
+                uint64_t v2[E2];
+                E::template load_pairs<C::CB>(sV + (size_t)r * C::ROWB + ch * C::CB, v2);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     const float pw = scr[h * RW + rl];
+                    const uint64_t p2 = pk2(pw, pw);
 #pragma unroll
-                    for (int e = 0; e < EPC; ++e) tmp[h][e] = fmaf(pw, vf[e], tmp[h][e]);
+                    for (int e = 0; e < E2; ++e) tN[h][e] = fma2(p2, v2[e], tN[h][e]);
                 }
             }
         }
         release();  // K, V and q of this slot are no longer read
 
-        int stop = 0;
         if (kART) {
-            // probe partials of this lane's rows: slot rank = columns of the probe before it
+            // probe partials of this lane's rows: slot rank = probe columns before it
             const int vb = v & 1;
             float* pp = part + (((size_t)vb * kNWC + w) * RPW + half) * G * kMaxProbe;
 #pragma unroll
@@ -672,73 +781,67 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
                 if ((my_mask >> e) & 1u) {
                     const int s = my_base + __popc(my_mask & ((1u << e) - 1u));
 #pragma unroll
-                    for (int h = 0; h < G; ++h) pp[h * kMaxProbe + s] = tmp[h][e];
+                    for (int h = 0; h < G; ++h) {
+                        float lo, hi;
+                        up2(tN[h][e >> 1], lo, hi);
+                        pp[h * kMaxProbe + s] = (e & 1) ? hi : lo;
+                    }
                 }
             }
             if (lane == 0) {
-                float* pm = pmeta + ((size_t)vb * kNWC + w) * 2 * G;
 #pragma unroll
-                for (int h = 0; h < G; ++h) { pm[h] = mbw[h]; pm[G + h] = lbw[h]; }
+                for (int h = 0; h < G; ++h) plb[(vb * kNWC + w) * G + h] = lbN[h];
             }
-        }
-        // ---- fold the block into this warp's running state (the block is always kept)
+            if (w == 0 && lane == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            if (mbw[h] != -INFINITY) {
-                const float mn = fmaxf(mrun[h], mbw[h]);
-                const float a = exp2f(mrun[h] - mn);
-                const float bb = exp2f(mbw[h] - mn);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) acc[h][e] = a * acc[h][e] + bb * tmp[h][e];
-                lrun[h] = a * lrun[h] + bb * lbw[h];
-                mrun[h] = mn;
+                for (int h = 0; h < G; ++h) pmb[vb * G + h] = mbN[h];
             }
-        }
-        if (kART) {
-            stop = publish_and_decide(mt);
-            if (stop < 0) return;
+            const int vN = publish(mt);
+            if (LAG) {
+                if (pending) {
+                    const int d = wait_dec(vP);
+                    if (d < 0) return;
+                    fold(tP, mbP, lbP);
+                    pending = false;
+                    if (d == kStop) {
+                        if (!epilogue(mP.b, mP.g)) return;
+                        reset();
+                        stopped_item = mP.item;
+                        if (mt.item == mP.item) {  // computed past the stop: wait for its discard
+                            if (wait_dec(vN) < 0) return;
+                            advance();
+                            continue;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    mbP[h] = mbN[h];
+                    lbP[h] = lbN[h];
+#pragma unroll
+                    for (int e = 0; e < E2; ++e) tP[h][e] = tN[h][e];
+                }
+                mP = mt;
+                vP = vN;
+                pending = true;
+                if (mt.pos == mt.n - 1 && !resolve_pending()) return;  // the last listed block
+            } else {
+                const int d = wait_dec(vN);
+                if (d < 0) return;
+                fold(tN, mbN, lbN);
+                if (d == kStop) {
+                    if (!epilogue(mt.b, mt.g)) return;
+                    reset();
+                    stopped_item = mt.item;
+                }
+            }
         } else {
-            stop = (mt.pos == mt.n - 1);
-        }
-
-        if (stop) {
-            // ---- epilogue: merge the row groups of each warp, then the warps
-#pragma unroll
-            for (int s = LPR; s < 32; s <<= 1)
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < EPC; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], s);
-            float* wacc = part;  // the probe partials are free once the last decision is made
-            if (half == 0) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < EPC; ++e) wacc[((size_t)w * G + h) * D + ch * EPC + e] = acc[h][e];
+            fold(tN, mbN, lbN);
+            if (mt.pos == mt.n - 1) {
+                if (!epilogue(mt.b, mt.g)) return;
+                reset();
+                stopped_item = mt.item;
             }
-            if (lane == 0) {
-#pragma unroll
-                for (int h = 0; h < G; ++h) { wml[(w * 2) * G + h] = mrun[h]; wml[(w * 2 + 1) * G + h] = lrun[h]; }
-            }
-            if (!cbar_sync()) return;
-            for (int idx = ctid; idx < G * D; idx += kNWC * 32) {
-                const int h = idx / D, col = idx - (idx / D) * D;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int ww = 0; ww < kNWC; ++ww) mx = fmaxf(mx, wml[(ww * 2) * G + h]);
-                float num = 0.f, den = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kNWC; ++ww) {
-                    const float mw = wml[(ww * 2) * G + h];
-                    const float e = mw == -INFINITY ? 0.f : exp2f(mw - mx);
-                    num += e * wacc[((size_t)ww * G + h) * D + col];
-                    den += e * wml[(ww * 2 + 1) * G + h];
-                }
-                E::store(p.out, out_ptr_index(mt.b, mt.g, h, col), num / den);
-            }
-            if (!cbar_sync()) return;
-            reset();
-            stopped_item = mt.item;
         }
         advance();
     }
@@ -747,13 +850,8 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int G>
-struct MinBlocks {
-    static constexpr int value = G <= 4 ? 2 : 1;
-};
-
 template <bool kBF16, int D, int G, bool kART>
-__global__ void __launch_bounds__(kThreads, MinBlocks<G>::value) art_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) art_decode_kernel(const Params p) {
     using C = Cfg<kBF16, D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout L = make_layout<C>(p.stages);
@@ -764,10 +862,6 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<G>::value) art_decode_kern
     uint64_t* part_full = empty + p.stages;
     uint64_t* dec_bar = part_full + 2;
     uint64_t* cbar = dec_bar + 2;
-    float* part = reinterpret_cast<float*>(smem + L.part);
-    float* pmeta = reinterpret_cast<float*>(smem + L.pmeta);
-    float* scr = reinterpret_cast<float*>(smem + L.scr);
-    float* wml = reinterpret_cast<float*>(smem + L.wml);
     int* pmask = reinterpret_cast<int*>(smem + L.ptab);
     int* pbase = pmask + C::LPR;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
@@ -809,25 +903,18 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<G>::value) art_decode_kern
     if (warp == kProducerWarp) {
         producer_warp<C, kART>(p, ring, meta, full, empty, ctrl);
     } else if (warp == kStatWarp) {
-        if (kART) stat_warp<C>(p, part, pmeta, part_full, dec_bar, ctrl);
+        if (kART)
+            stat_warp<C>(p, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
+                         reinterpret_cast<const float*>(smem + L.pmb), reinterpret_cast<float*>(smem + L.sh),
+                         part_full, dec_bar, ctrl);
     } else {
-        consumer_warps<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, part, pmeta, scr, wml,
-                                pmask, pbase, ctrl);
+        consumer_warps<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, pmask, pbase, ctrl);
     }
 }
 
-}  // namespace art
-
-namespace art {
-
-// Largest ring depth (2..8 slots) whose shared memory still lets `want` CTAs
-// share one SM. Returns 0 when not even two slots fit one CTA.
+// Largest ring depth (2..8 slots) that fits one CTA per SM.
 template <class C>
-inline int pick_stages(int want, int smem_per_sm, int smem_per_block) {
-    for (int s = 8; s >= 2; --s) {
-        const size_t t = make_layout<C>(s).total;
-        if ((int)t <= smem_per_block && (size_t)want * (t + 1024) <= (size_t)smem_per_sm) return s;
-    }
+inline int pick_stages(int smem_per_block) {
     for (int s = 8; s >= 2; --s)
         if ((int)make_layout<C>(s).total <= smem_per_block) return s;
     return 0;
@@ -840,16 +927,14 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int sms = 0, smem_sm = 0, smem_blk = 0;
+    int sms = 0, smem_blk = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
-        return e;
     if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    int stages = force_stages >= 2 && force_stages <= 8 ? force_stages
-                                                          : pick_stages<C>(MinBlocks<G>::value, smem_sm, smem_blk);
+    const int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(smem_blk);
     if (stages == 0) return cudaErrorInvalidConfiguration;
     const size_t smem = make_layout<C>(stages).total;
+    if ((int)smem > smem_blk) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
     int occ = 0;

@@ -118,7 +118,7 @@ SHAPES = [
 def test_shapes(spec):
     dt, d, hq, hkv, ps, lens, order = spec
     w = W.build("shape", seed=31, dtype=dt, batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
-                page_size=ps, block_size=64, seq_lens=lens, paged="permuted", order=order, v_boost_frac=0.1)
+                page_size=ps, block_size=64, seq_lens=lens, paged="permuted", order=order)
     out, _, st, dev = run_gpu(w, "dense")
     assert st == 0
     check_dense(w, out, what=f"dense {spec}")
