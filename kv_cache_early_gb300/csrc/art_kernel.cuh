@@ -40,6 +40,8 @@
 // the CTA returns.
 #pragma once
 
+#include <cstring>
+
 #include "art_common.cuh"
 
 namespace art {
@@ -57,6 +59,9 @@ enum Decision : int { kContinue = 0, kStop = 1, kDiscard = 2 };
 template <bool kBF16, int D, int G>
 struct Cfg {
     using E = Elem<kBF16>;
+    static constexpr bool TC = kBF16;            // bf16: tensor-core consumers on swizzled tiles
+    static constexpr int NWC = TC ? 4 : 8;       // consumer warps
+    static constexpr int THREADS = (NWC + 2) * 32;
     static constexpr int GQ = G;                 // query heads per KV head
     static constexpr int ELT = E::kBytes;
     static constexpr int DD = D;
@@ -66,19 +71,21 @@ struct Cfg {
     static constexpr int E2 = EPC / 2;           // packed pairs per chunk
     static constexpr int LPR = ROWB / CB;        // lanes covering one row
     static constexpr int RPW = 32 / LPR;         // rows per warp instruction
-    static constexpr int RW = kBK / kNWC;        // rows per consumer warp per block
+    static constexpr int RW = kBK / NWC;         // rows per consumer warp per block
     static constexpr int NI = RW / RPW;          // warp instructions per block
     static constexpr int NV = NI * G;            // partial scores per lane
     static constexpr int NVP = pow2ceil(imax(NV, LPR));
     static constexpr int QB = (int)align_up((size_t)G * D * ELT, 16);
     static constexpr int KVB = kBK * ROWB;       // bytes of K (or V) of one block
-    static constexpr int SLOT = 2 * KVB + QB;
+    static constexpr int SLOT = (int)align_up((size_t)2 * KVB + QB, TC ? 1024 : 16);
     static constexpr int SPL = (G * kMaxProbe + 31) / 32;  // probe slots per stat lane
-    static constexpr int PART_F = 2 * kNWC * RPW * G * kMaxProbe;
+    static constexpr int PRW = TC ? 1 : RPW;     // probe partial rows per warp
+    static constexpr int PART_F = 2 * NWC * PRW * G * kMaxProbe;
+    static constexpr int KS = D / 16;            // tensor-core k-steps (QK) and m-tiles (PV)
     static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
     static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
     static_assert(RW % RPW == 0 && NI >= 1, "rows per warp");
-    static_assert(32 % RW == 0, "softmax lane groups");
+    static_assert(TC || 32 % RW == 0, "softmax lane groups");
     static_assert(G >= 1 && G <= 8, "group size");
 };
 
@@ -94,7 +101,7 @@ struct Ctrl {
 };
 
 struct Layout {
-    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, sh, ptab, ctrl, total;
+    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, sh, ptab, ctrl, total;
 };
 
 template <class C>
@@ -111,26 +118,29 @@ __host__ __device__ inline Layout make_layout(int stages) {
     L.part = o;  // [2][NWC][RPW][G][kMaxProbe] probe partials
     o += (size_t)C::PART_F * sizeof(float);
     L.plb = o;  // [2][NWC][G] per-warp block sums
-    o += (size_t)2 * kNWC * G * sizeof(float);
+    o += (size_t)2 * C::NWC * G * sizeof(float);
     L.pmb = o;  // [2][G] block maxima
     o += (size_t)2 * G * sizeof(float);
-    L.wmax = o;  // [NWC][G] per-warp maxima of the block being processed
-    o += (size_t)kNWC * G * sizeof(float);
+    L.wmax = o;  // [2][NWC][8] per-warp maxima of the block being processed (by block parity)
+    o += (size_t)2 * C::NWC * 8 * sizeof(float);
     L.scr = o;  // [NWC][G][RW] scores, then weights
-    o += (size_t)kNWC * G * C::RW * sizeof(float);
+    o += (size_t)C::NWC * G * C::RW * sizeof(float);
     o = align_up(o, 16);
     L.eacc = o;  // per consumer warp: [G][D] output sums, then [G] weight sums
-    o += (size_t)kNWC * (G * C::DD + G) * sizeof(float);
+    o += (size_t)C::NWC * (G * C::DD + G) * sizeof(float);
+    o = align_up(o, 1024);
+    L.qt = o;  // tensor-core path: the item's queries, 8 rows (heads past G zero), 128B-swizzled
+    o += C::TC ? (size_t)8 * C::ROWB : 0;
     o = align_up(o, 16);
     L.sh = o;  // [3][G] statistics warp scratch
     o += (size_t)3 * G * sizeof(float);
     o = align_up(o, 16);
-    L.ptab = o;
-    o += (size_t)2 * C::LPR * sizeof(int);
+    L.ptab = o;  // CUDA-core path: mask and base per chunk; tensor-core path: rank per column
+    o += (size_t)(2 * C::LPR + C::DD) * sizeof(int);
     o = align_up(o, 16);
     L.ctrl = o;
     o += sizeof(Ctrl);
-    L.total = align_up(o, 128);
+    L.total = align_up(o, 128) + (C::TC ? 1024 : 0);  // room to align the ring to 1024 bytes
     return L;
 }
 
@@ -162,13 +172,16 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Waits for the phase with `parity` of `bar` to complete, warp-uniformly.
-// Returns false when the CTA is aborting or the wait exceeded kWaitLimitNs.
+// Waits for the phase with `parity` of `bar` to complete, warp-uniformly. The
+// threads sleep in mbarrier.try_wait (woken by the phase completing) rather
+// than spin. Returns false when the CTA is aborting or the wait exceeded
+// kWaitLimitNs.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctrl* ctrl, WsHeader* hdr) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    constexpr uint32_t kSleepNs = 200000;  // upper bound of one sleep; the limit is checked between sleeps
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
         int stop = ld_volatile_shared(&ctrl->abort);
         if (!stop && (threadIdx.x & 31) == 0 && global_ns() - t0 > kWaitLimitNs) {
             st_volatile_shared(&ctrl->abort, 1);
@@ -184,7 +197,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctr
 // ---------------------------------------------------------------------------
 template <class C, bool kART>
 __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* meta, uint64_t* full,
-                              uint64_t* empty, Ctrl* ctrl) {
+                              uint64_t* empty, Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv) {
     constexpr int G = C::GQ;
     const int lane = threadIdx.x & 31;
     int slot = 0;
@@ -307,6 +320,30 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                     mbar_arrive_expect_tx(&full[slot], bytes);
                 }
                 __syncwarp();
+                if constexpr (C::TC) {
+                    // 128-byte column boxes of each page, written 128B-swizzled by the tensor maps
+                    constexpr int NH = C::ROWB / 128;
+                    const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
+                    const int nbox = 2 * npj * NH;
+                    for (int t = lane; t < nbox + (with_q ? 1 : 0); t += 32) {
+                        if (t < nbox) {
+                            const int kv = t / (npj * NH);
+                            const int rem = t - kv * npj * NH;
+                            const int k = rem / NH, hf = rem - (rem / NH) * NH;
+                            int pk = 0;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                if (u == k) pk = pgj[u];
+                            const int y = (pk * p.Hkv + g) * p.Ps + r0j;
+                            unsigned char* d = dst + kv * C::KVB + hf * (kBK * 128) + k * page_rows * 128;
+                            tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
+                        } else {
+                            const char* src =
+                                static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
+                            bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
+                        }
+                    }
+                } else {
                 const int ncopy = 2 * npj + (with_q ? 1 : 0);
                 if (lane < ncopy) {
                     if (lane < 2 * npj) {
@@ -323,6 +360,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                         const char* src = static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
                         bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
                     }
+                }
                 }
                 __syncwarp();
                 advance();
@@ -354,21 +392,21 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
                           uint64_t* part_full, uint64_t* dec_bar, Ctrl* ctrl) {
     constexpr int G = C::GQ;
     constexpr int SPL = C::SPL;
-    constexpr int RPW = C::RPW;
+    constexpr int NP = C::NWC * C::PRW;  // partial rows per probe slot
     const int lane = threadIdx.x & 31;
     const int m = p.m;
     const int GM = G * m;
-    // the probe slot of each (lane, j): head and column rank
-    int hs[SPL], ss[SPL];
+    // the probe slot of each (lane, j): head, and its offset in a partial row
+    int hs[SPL], off[SPL];
 #pragma unroll
     for (int j = 0; j < SPL; ++j) {
         const int k = lane + 32 * j;
         hs[j] = k < GM ? k / m : -1;
-        ss[j] = k < GM ? k - (k / m) * m : 0;
+        off[j] = k < GM ? (k / m) * kMaxProbe + (k - (k / m) * m) : 0;
     }
     float Mh = -INFINITY, Lh = 0.f;  // running max / sum of head `lane` (lanes < G)
-    float X[SPL], dl[SPL];
-    float nprev = 0.f;
+    float X[SPL];
+    float n2prev = 0.f;               // |x_{i-1}|^2
     int counter = 0, seen0 = 0;
     int stopped_item = -1;
     auto reset = [&]() {
@@ -376,7 +414,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         Lh = 0.f;
 #pragma unroll
         for (int j = 0; j < SPL; ++j) X[j] = 0.f;
-        nprev = 0.f;
+        n2prev = 0.f;
         counter = 0;
         seen0 = 0;
     };
@@ -384,87 +422,85 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
     for (int v = 0;; ++v) {
         const int vb = v & 1;
         if (!wait_bounded(&part_full[vb], (uint32_t)(v >> 1) & 1u, ctrl, p.hdr)) return;
-        const SlotMeta info = ctrl->info[vb];
-        if (info.kind == kSlotEnd) return;
+        const SlotMeta* info = &ctrl->info[vb];
+        const int kind = info->kind, item = info->item;
         int dec = kStop;
-        if (info.kind != kSlotBlock) {
-            if (lane == 0) p.blocks_used[info.item] = info.kind == kSlotFail ? -1 : 0;
+        if (kind == kSlotEnd) return;
+        if (kind != kSlotBlock) {
+            if (lane == 0) p.blocks_used[item] = kind == kSlotFail ? -1 : 0;
             reset();
-        } else if (info.item == stopped_item) {
+        } else if (item == stopped_item) {
             dec = kDiscard;  // computed ahead of the decision that stopped its item
         } else {
-            if (info.pos == 0) reset();
-            // per head: block sum over the warps, new running max and sum
+            const int pos = info->pos, n = info->n, c = info->c, has0 = info->has0;
+            if (pos == 0) reset();
+            // per head (lane h < G): block sum, new running max and sum; the probe of
+            // head h moves by delta = coef_h * (PV_probe - l_blk,h * x)
             if (lane < G) {
                 const float mb = pmb[vb * G + lane];
                 float lb = 0.f;
 #pragma unroll
-                for (int w = 0; w < kNWC; ++w) lb += plb[(vb * kNWC + w) * G + lane];
+                for (int w = 0; w < C::NWC; ++w) lb += plb[(vb * C::NWC + w) * G + lane];
                 const float Mn = fmaxf(Mh, mb);
                 const float a = exp2f(Mh - Mn);
                 const float bw = exp2f(mb - Mn);
                 const float Ln = a * Lh + bw * lb;
-                sh[lane] = bw;
+                sh[lane] = bw / Ln;
                 sh[G + lane] = lb;
-                sh[2 * G + lane] = Ln;
                 Mh = Mn;
                 Lh = Ln;
             }
             __syncwarp();
-            const float* pp = part + (size_t)vb * kNWC * RPW * G * kMaxProbe;
-            float sx2 = 0.f, sdd = 0.f;
+            const float* pp = part + (size_t)vb * NP * G * kMaxProbe;
+            float s1 = 0.f, s2 = 0.f, s3 = 0.f;  // sum delta^2, sum delta . x_{i-1}, |x_i|^2
 #pragma unroll
             for (int j = 0; j < SPL; ++j) {
-                dl[j] = 0.f;
                 const int h = hs[j];
                 if (h >= 0) {
                     float pb = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kNWC * RPW; ++w) pb += pp[(w * G + h) * kMaxProbe + ss[j]];
-                    const float d = sh[h] * (pb - sh[G + h] * X[j]) / sh[2 * G + h];
-                    dl[j] = d;
-                    const float x = X[j] + d;
-                    sx2 += x * x;
-                    sdd += d * (2.f * X[j] + d);
+                    for (int w = 0; w < NP; ++w) pb += pp[w * G * kMaxProbe + off[j]];
+                    const float d = sh[h] * (pb - sh[G + h] * X[j]);
+                    s1 = fmaf(d, d, s1);
+                    s2 = fmaf(d, X[j], s2);
+                    X[j] += d;
+                    s3 = fmaf(X[j], X[j], s3);
                 }
             }
-            sx2 = warp_sum(sx2);
-            sdd = warp_sum(sdd);
-            const float ni = sqrtf(sx2);
-            const float dn = sdd / (ni + nprev);
-            bool stable = false;
-            if (info.pos >= 1) {
-                float su2 = 0.f;
-                const float cx = dn / (ni * nprev);
 #pragma unroll
-                for (int j = 0; j < SPL; ++j) {
-                    if (hs[j] >= 0) {
-                        const float u = dl[j] / ni - X[j] * cx;
-                        su2 += u * u;
-                    }
-                }
-                su2 = warp_sum(su2);
+            for (int o = 16; o >= 1; o >>= 1) {
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+                s3 += __shfl_xor_sync(0xffffffffu, s3, o);
+            }
+            // |x_i| - |x_{i-1}| = (|x_i|^2 - |x_{i-1}|^2) / (|x_i| + |x_{i-1}|) with the
+            // difference of squares formed directly as 2 s2 + s1;
+            // 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2 = (s1 - 2 s2 dn / n_{i-1} + dn^2) / (2 |x_i|^2)
+            const float nprev = sqrtf(n2prev);
+            const float g2 = 2.f * s2 + s1;
+            const float n2 = s3;
+            const float ni = sqrtf(n2);
+            bool stable = false;
+            if (pos >= 1) {
+                const float dn = g2 / (ni + nprev);
                 const float dmag = fabsf(dn) / nprev;
-                const float ddir = 0.5f * su2;
+                const float ddir = fmaxf(0.f, (s1 - 2.f * s2 * (dn / nprev) + dn * dn) / (2.f * n2));
                 stable = nprev > 0.f && ni > 0.f && isfinite(nprev) && isfinite(ni) && isfinite(dmag) &&
                          isfinite(ddir) && dmag < p.eps_mag && ddir < p.eps_dir;
             }
+            n2prev = n2;
             counter = stable ? counter + 1 : 0;
-            if (info.c == 0) seen0 = 1;
-            const bool stop = ((counter >= p.patience) && (seen0 || !info.has0)) || (info.pos == info.n - 1);
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) X[j] += dl[j];
-            nprev = ni;
+            if (c == 0) seen0 = 1;
+            const bool stop = ((counter >= p.patience) && (seen0 || !has0)) || (pos == n - 1);
             dec = stop ? kStop : kContinue;
             if (stop) {
-                stopped_item = info.item;
+                stopped_item = item;
                 if (lane == 0) {
-                    p.blocks_used[info.item] = info.pos + 1;
-                    st_volatile_shared(&ctrl->stop_item, info.item);
+                    p.blocks_used[item] = pos + 1;
+                    st_volatile_shared(&ctrl->stop_item, item);
                 }
             }
         }
-        __syncwarp();
         if (lane == 0) {
             ctrl->dec[vb] = dec;
             mbar_arrive(&dec_bar[vb]);
@@ -484,6 +520,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     constexpr int G = C::GQ;
     constexpr int EPC = C::EPC, E2 = C::E2, LPR = C::LPR, RPW = C::RPW, RW = C::RW, NI = C::NI;
     constexpr int D = C::DD;
+    constexpr int kNWC = C::NWC;
     constexpr bool LAG = kART && C::LAG;
     using E = typename C::E;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -530,6 +567,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     uint32_t round = 0;
     int v = 0;          // records published to the statistics warp
     uint32_t cbph = 0;  // consumer-barrier phase
+    int bpar = 0;       // parity of the blocks computed (selects the wmax buffer)
     int stopped_item = -1;
 
     auto cbar_sync = [&]() -> bool {
@@ -714,20 +752,21 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
             float mx = h < G ? scr[h * RW + rl] : -INFINITY;
 #pragma unroll
             for (int o = RW / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (h < G && rl == 0) wmax[w * G + h] = mx;
+            if (h < G && rl == 0) wmax[(bpar * kNWC + w) * 8 + h] = mx;
         }
         named_bar_sync(1, kNWC * 32);
 #pragma unroll
         for (int k = 0; k < (G * kNWC + 31) / 32; ++k) {
             const int idx = k * 32 + lane;
             const int h = idx / kNWC, ww = idx % kNWC;
-            float mx = h < G ? wmax[ww * G + h] : -INFINITY;
+            float mx = h < G ? wmax[(bpar * kNWC + ww) * 8 + h] : -INFINITY;
 #pragma unroll
             for (int o = kNWC / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 #pragma unroll
             for (int hh = 0; hh < G; ++hh)
                 if (hh / (32 / kNWC) == k) mbN[hh] = __shfl_sync(0xffffffffu, mx, (hh % (32 / kNWC)) * kNWC);
         }
+        bpar ^= 1;
         // ---- weights and this warp's block sums
 #pragma unroll
         for (int k = 0; k < (G * RW + 31) / 32; ++k) {
@@ -847,13 +886,402 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// tensor-core consumer warps (bf16). Warp w owns keys 16w .. 16w+15 of the
+// block. S^T (16 keys x 8 heads) = K (16 x d) . Q^T (d x 8) with
+// mma.m16n8k16, K fragments by ldmatrix from the 128B-swizzled tile; the
+// weights are split into bf16 hi + lo parts (p = hi + lo to ~2^-17) and
+// O^T (d x 8 heads) += V^T (d x 16 keys) . P^T (16 keys x 8 heads), V^T
+// fragments by ldmatrix.trans, P^T fragments by movmatrix of the S^T layout.
+// Heads beyond G are carried as zeros.
+// ---------------------------------------------------------------------------
+template <class C, bool kART>
+__device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta* meta, uint64_t* full,
+                            uint64_t* empty, uint64_t* part_full, uint64_t* dec_bar, uint64_t* cbar, const Layout& L,
+                            unsigned char* smem, const int* prank, Ctrl* ctrl) {
+    constexpr int G = C::GQ, D = C::DD, KS = C::KS, NWC = C::NWC;
+    constexpr bool LAG = kART && C::LAG;
+    using E = typename C::E;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 2, tig = lane & 3;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    const bool v0 = h0 < G, v1 = h1 < G;
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    float* plb = reinterpret_cast<float*>(smem + L.plb);
+    float* pmb = reinterpret_cast<float*>(smem + L.pmb);
+    float* wmax = reinterpret_cast<float*>(smem + L.wmax);
+    float* eacc = reinterpret_cast<float*>(smem + L.eacc);
+    const float scale = 1.4426950408889634f / sqrtf((float)D);
+    const int ctid = threadIdx.x;
+    // this lane's O^T rows are d = 16 mt + grp + 8 r; bit 2 mt + r marks a probe column,
+    // byte 2 mt + r of prk holds its rank among the probe columns
+    uint32_t pbits = 0;
+    uint32_t prk[(2 * KS + 3) / 4];
+#pragma unroll
+    for (int i = 0; i < (2 * KS + 3) / 4; ++i) prk[i] = 0;
+    if (kART) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int rk = prank[16 * mt + grp + 8 * r];
+                if (rk >= 0) {
+                    pbits |= 1u << (2 * mt + r);
+                    prk[(2 * mt + r) >> 2] |= (uint32_t)rk << (8 * ((2 * mt + r) & 3));
+                }
+            }
+    }
+    const int mi = lane >> 3, lr = lane & 7;
+    const int keyK = w * 16 + (mi & 1) * 8 + lr;   // K rows for the S^T A fragments
+    const int chK = mi >> 1;
+    const int keyV = w * 16 + (mi >> 1) * 8 + lr;  // V rows for the O^T A fragments
+    const int chV = mi & 1;
+    auto sw = [](uint32_t base, int row, int chunk) -> uint32_t {
+        return base + (uint32_t)((chunk >> 3) * (kBK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    };
+
+    float acc[KS][4], tN[KS][4], tP[KS][4];
+    unsigned char* sQt = smem + L.qt;
+    const uint32_t qtbase = smem_addr(sQt);
+    float mrun[2], lrun[2], mbN[2], lbN[2], mbP[2], lbP[2];
+    int itemP = -1, bP = 0, gP = 0;  // item of the pending block
+    int vP = 0;
+    bool pending = false;
+    auto reset = [&]() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) { mrun[j] = -INFINITY; lrun[j] = 0.f; }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
+    };
+    reset();
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tN[mt][c] = tP[mt][c] = 0.f;
+    mbN[0] = mbN[1] = mbP[0] = mbP[1] = lbN[0] = lbN[1] = lbP[0] = lbP[1] = 0.f;
+
+    int slot = 0;
+    uint32_t round = 0;
+    int v = 0;
+    uint32_t cbph = 0;
+    int bpar = 0;
+    int stopped_item = -1;
+
+    auto cbar_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cbar);
+        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr);
+        cbph ^= 1u;
+        return r;
+    };
+    auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    };
+    auto advance = [&]() {
+        if (++slot == p.stages) { slot = 0; ++round; }
+    };
+    auto out_index = [&](int b, int g, int h, int col) -> size_t {
+        return ((size_t)b * p.Hq + (size_t)g * G + h) * D + col;
+    };
+    auto publish = [&](const SlotMeta& mt) -> int {
+        const int vb = v & 1;
+        if (w == 0 && lane == 0) {
+            SlotMeta& r = ctrl->info[vb];
+            r.kind = mt.kind; r.item = mt.item; r.pos = mt.pos; r.n = mt.n; r.c = mt.c; r.has0 = mt.has0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&part_full[vb]);
+        return v++;
+    };
+    auto wait_dec = [&](int rec) -> int {
+        if (!wait_bounded(&dec_bar[rec & 1], (uint32_t)(rec >> 1) & 1u, ctrl, p.hdr)) return -1;
+        return ctrl->dec[rec & 1];
+    };
+    auto fold = [&](const float (&t)[KS][4], const float* mb, const float* lb) {
+        float a[2], bb[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (mb[j] == -INFINITY) {  // a head beyond G
+                a[j] = 1.f;
+                bb[j] = 0.f;
+                continue;
+            }
+            const float mn = fmaxf(mrun[j], mb[j]);
+            a[j] = exp2f(mrun[j] - mn);
+            bb[j] = exp2f(mb[j] - mn);
+            lrun[j] = a[j] * lrun[j] + bb[j] * lb[j];
+            mrun[j] = mn;
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][c] = a[c & 1] * acc[mt][c] + bb[c & 1] * t[mt][c];
+    };
+    auto epilogue = [&](int b, int g) -> bool {
+        float* mine = eacc + (size_t)w * (G * D + G);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int d = 16 * mt + grp + 8 * r;
+                if (v0) mine[h0 * D + d] = acc[mt][2 * r];
+                if (v1) mine[h1 * D + d] = acc[mt][2 * r + 1];
+            }
+        if (grp == 0) {
+            if (v0) mine[G * D + h0] = lrun[0];
+            if (v1) mine[G * D + h1] = lrun[1];
+        }
+        if (!cbar_sync()) return false;
+        for (int idx = ctid; idx < G * D; idx += NWC * 32) {
+            const int h = idx / D, col = idx - (idx / D) * D;
+            float num = 0.f, den = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NWC; ++ww) {
+                num += eacc[(size_t)ww * (G * D + G) + idx];
+                den += eacc[(size_t)ww * (G * D + G) + G * D + h];
+            }
+            E::store(p.out, out_index(b, g, h, col), num / den);
+        }
+        return cbar_sync();
+    };
+    auto write_zero = [&](int b, int g) {
+        for (int idx = ctid; idx < G * D; idx += NWC * 32) E::store(p.out, out_index(b, g, idx / D, idx % D), 0.f);
+    };
+    auto resolve_pending = [&]() -> bool {
+        const int d = wait_dec(vP);
+        if (d < 0) return false;
+        fold(tP, mbP, lbP);
+        pending = false;
+        if (d == kStop) {
+            if (!epilogue(bP, gP)) return false;
+            reset();
+            stopped_item = itemP;
+        }
+        return true;
+    };
+
+    for (;;) {
+        if (!wait_bounded(&full[slot], round & 1u, ctrl, p.hdr)) return;
+        const SlotMeta mt = meta[slot];
+        if (mt.kind == kSlotEnd) {
+            if (LAG && pending && !resolve_pending()) return;
+            if (kART) publish(mt);
+            return;
+        }
+        if (mt.kind != kSlotBlock) {
+            release();
+            if (LAG && pending && !resolve_pending()) return;
+            if (mt.item != stopped_item) {
+                write_zero(mt.b, mt.g);
+                if (kART && wait_dec(publish(mt)) < 0) return;
+                reset();
+                stopped_item = mt.item;
+            }
+            advance();
+            continue;
+        }
+        if (mt.item == stopped_item) {
+            release();
+            advance();
+            continue;
+        }
+        unsigned char* sK = ring + (size_t)slot * C::SLOT;
+        unsigned char* sV = sK + C::KVB;
+        if (mt.pos == 0) {
+            // the item's queries into the swizzled 8-row area (rows past G zero); every warp
+            // has finished the previous item's scores before the barrier of its last block
+            const unsigned char* sQ = sK + 2 * C::KVB;
+            constexpr int QCH = 8 * (C::ROWB / 16);
+            for (int i = ctid; i < QCH; i += NWC * 32) {
+                const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
+            }
+            named_bar_sync(1, NWC * 32);
+        }
+        const int nvalid = mt.nvalid;
+
+        // ---- S^T for this warp's 16 keys
+        float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};  // two independent chains
+        const uint32_t kbase = smem_addr(sK), vbase = smem_addr(sV);
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp) {
+            // B fragments (Q^T) of k-steps 2kp and 2kp+1: rows = heads, 8 columns each
+            uint32_t b00, b01, b10, b11;
+            {
+                const int c = 4 * kp + mi;
+                ldsm_x4(qtbase + (uint32_t)((c >> 3) * 1024 + lr * 128 + (((c & 7) ^ lr) << 4)), b00, b01, b10, b11);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ks = 2 * kp + h;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sw(kbase, keyK, 2 * ks + chK), a0, a1, a2, a3);
+                mma_bf16(h ? s4b : s4, a0, a1, a2, a3, h ? b10 : b00, h ? b11 : b01);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s4[c] += s4b[c];
+        const int k0 = w * 16 + grp, k1 = k0 + 8;
+        float sc[4];
+        sc[0] = (k0 < nvalid && v0) ? s4[0] * scale : -INFINITY;
+        sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
+        sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
+        sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
+        // ---- block max per head: over this warp's keys, then across the warps
+        float m0 = fmaxf(sc[0], sc[2]), m1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        }
+        if (grp == 0) {
+            wmax[(bpar * NWC + w) * 8 + h0] = m0;
+            wmax[(bpar * NWC + w) * 8 + h1] = m1;
+        }
+        named_bar_sync(1, NWC * 32);
+        float mb0 = -INFINITY, mb1 = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < NWC; ++ww) {
+            mb0 = fmaxf(mb0, wmax[(bpar * NWC + ww) * 8 + h0]);
+            mb1 = fmaxf(mb1, wmax[(bpar * NWC + ww) * 8 + h1]);
+        }
+        bpar ^= 1;
+        float pw[4];
+        pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mb0);
+        pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mb1);
+        pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - mb0);
+        pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - mb1);
+        float l0 = pw[0] + pw[2], l1 = pw[1] + pw[3];
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+        mbN[0] = mb0; mbN[1] = mb1; lbN[0] = l0; lbN[1] = l1;
+        // ---- P^T fragments: hi and lo bf16 parts, transposed by movmatrix
+        const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
+        const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
+        const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
+        const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB), bl0 = movm_t(lA), bl1 = movm_t(lB);
+        // ---- rows past the sequence end hold stale data: zero this warp's, so 0 * V stays 0
+        if (nvalid < w * 16 + 16) {
+            const int r0 = max(nvalid, w * 16);
+            const int nchunks = (w * 16 + 16 - r0) * (C::ROWB / 16);
+            for (int i = lane; i < nchunks; i += 32) {
+                const int row = r0 + i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                *reinterpret_cast<uint4*>(sV + (c >> 3) * (kBK * 128) + row * 128 + (c & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        // ---- O^T partial of this block
+#pragma unroll
+        for (int m = 0; m < KS; ++m) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(sw(vbase, keyV, 2 * m + chV), a0, a1, a2, a3);
+            tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
+            mma_bf16(tN[m], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
+        }
+        release();
+
+        if (kART) {
+            // probe partials of this block, then the record for the statistics warp
+            auto publish_block = [&]() -> int {
+                const int vb = v & 1;
+                float* pp = part + ((size_t)vb * NWC + w) * G * kMaxProbe;
+#pragma unroll
+                for (int m = 0; m < KS; ++m)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const bool on = (pbits >> (2 * m + r)) & 1u;
+                        const int rank = (int)((prk[(2 * m + r) >> 2] >> (8 * ((2 * m + r) & 3))) & 0xffu);
+                        if (on && v0) pp[h0 * kMaxProbe + rank] = tN[m][2 * r];
+                        if (on && v1) pp[h1 * kMaxProbe + rank] = tN[m][2 * r + 1];
+                    }
+                if (grp == 0) {
+                    if (v0) plb[(vb * NWC + w) * G + h0] = l0;
+                    if (v1) plb[(vb * NWC + w) * G + h1] = l1;
+                    if (w == 0) {
+                        if (v0) pmb[vb * G + h0] = mb0;
+                        if (v1) pmb[vb * G + h1] = mb1;
+                    }
+                }
+                return publish(mt);
+            };
+            if (LAG) {
+                // the previous block's decision (computed during this block) decides it
+                if (pending) {
+                    const int d = wait_dec(vP);
+                    if (d < 0) return;
+                    fold(tP, mbP, lbP);
+                    pending = false;
+                    if (d == kStop) {
+                        if (!epilogue(bP, gP)) return;
+                        reset();
+                        stopped_item = itemP;
+                        if (mt.item == itemP) {  // computed past the stop: dropped, never published
+                            advance();
+                            continue;
+                        }
+                    }
+                }
+                const int vN = publish_block();
+#pragma unroll
+                for (int m = 0; m < KS; ++m)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tP[m][c] = tN[m][c];
+                mbP[0] = mbN[0]; mbP[1] = mbN[1]; lbP[0] = lbN[0]; lbP[1] = lbN[1];
+                itemP = mt.item; bP = mt.b; gP = mt.g;
+                vP = vN;
+                pending = true;
+                if (mt.pos == mt.n - 1 && !resolve_pending()) return;
+            } else {
+                const int d = wait_dec(publish_block());
+                if (d < 0) return;
+                fold(tN, mbN, lbN);
+                if (d == kStop) {
+                    if (!epilogue(mt.b, mt.g)) return;
+                    reset();
+                    stopped_item = mt.item;
+                }
+            }
+        } else {
+            fold(tN, mbN, lbN);
+            if (mt.pos == mt.n - 1) {
+                if (!epilogue(mt.b, mt.g)) return;
+                reset();
+                stopped_item = mt.item;
+            }
+        }
+        advance();
+    }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+template <bool kBF16, int D, int G>
+struct MinBlocks {
+    static constexpr int value = Cfg<kBF16, D, G>::TC ? 2 : 1;
+};
+
 template <bool kBF16, int D, int G, bool kART>
-__global__ void __launch_bounds__(kThreads, 1) art_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(Cfg<kBF16, D, G>::THREADS, (MinBlocks<kBF16, D, G>::value))
+    art_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
     using C = Cfg<kBF16, D, G>;
-    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int NWC = C::NWC;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the swizzled tiles need a 1024-byte aligned ring
+    unsigned char* smem = smem_raw;
+    if (C::TC) smem += (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     const Layout L = make_layout<C>(p.stages);
     unsigned char* ring = smem;
     SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + L.meta);
@@ -864,19 +1292,20 @@ __global__ void __launch_bounds__(kThreads, 1) art_decode_kernel(const Params p)
     uint64_t* cbar = dec_bar + 2;
     int* pmask = reinterpret_cast<int*>(smem + L.ptab);
     int* pbase = pmask + C::LPR;
+    int* prank = pbase + C::LPR;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
 
     const int tid = threadIdx.x;
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kNWC);
+            mbar_init(&empty[s], NWC);
         }
-        mbar_init(&part_full[0], kNWC);
-        mbar_init(&part_full[1], kNWC);
+        mbar_init(&part_full[0], NWC);
+        mbar_init(&part_full[1], NWC);
         mbar_init(&dec_bar[0], 1);
         mbar_init(&dec_bar[1], 1);
-        mbar_init(cbar, kNWC);
+        mbar_init(cbar, NWC);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
         ctrl->dec[0] = ctrl->dec[1] = 0;
@@ -897,27 +1326,78 @@ __global__ void __launch_bounds__(kThreads, 1) art_decode_kernel(const Params p)
         pmask[tid] = (int)mask;
         pbase[tid] = base;
     }
+    if (tid < D) {
+        // rank of column `tid` among the probe columns, or -1
+        int found = 0, rank = 0;
+        if (kART && p.probe) {
+            for (int k = 0; k < p.m; ++k) {
+                const int col = __ldg(&p.probe[k]);
+                if (col == tid) found = 1;
+                if (col >= 0 && col < tid) ++rank;
+            }
+        }
+        prank[tid] = found ? rank : -1;
+    }
+    if (C::TC && tid == NWC * 32) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+    }
     __syncthreads();
 
     const int warp = tid >> 5;
-    if (warp == kProducerWarp) {
-        producer_warp<C, kART>(p, ring, meta, full, empty, ctrl);
-    } else if (warp == kStatWarp) {
+    if (warp == NWC) {
+        producer_warp<C, kART>(p, ring, meta, full, empty, ctrl, &tk, &tv);
+    } else if (warp == NWC + 1) {
         if (kART)
             stat_warp<C>(p, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
                          reinterpret_cast<const float*>(smem + L.pmb), reinterpret_cast<float*>(smem + L.sh),
                          part_full, dec_bar, ctrl);
+    } else if constexpr (C::TC) {
+        consumer_tc<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, prank, ctrl);
     } else {
         consumer_warps<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, pmask, pbase, ctrl);
     }
 }
 
-// Largest ring depth (2..8 slots) that fits one CTA per SM.
+// Largest ring depth (2..8 slots) that lets `want` CTAs share one SM.
 template <class C>
-inline int pick_stages(int smem_per_block) {
-    for (int s = 8; s >= 2; --s)
-        if ((int)make_layout<C>(s).total <= smem_per_block) return s;
+inline int pick_stages(int want, int smem_per_sm, int smem_per_block) {
+    for (int s = 8; s >= 2; --s) {
+        const size_t t = make_layout<C>(s).total;
+        if ((int)t <= smem_per_block && (size_t)want * (t + 1024) <= (size_t)smem_per_sm) return s;
+    }
     return 0;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// A 2-D bf16 view [rows = pages * Hkv * page_size][D] of a cache, read in
+// boxes of 64 columns (128 bytes) by min(page_size, 64) rows, 128B-swizzled.
+inline cudaError_t make_cache_map(CUtensorMap* m, const void* base, long long rows, int D, int Ps) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(Ps < kBK ? Ps : kBK)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <bool kBF16, int D, int G, bool kART>
@@ -927,24 +1407,38 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int sms = 0, smem_blk = 0;
+    int sms = 0, smem_sm = 0, smem_blk = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+        return e;
     if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    const int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(smem_blk);
+    // two CTAs per SM only pay when there are items for both
+    const int want = (MinBlocks<kBF16, D, G>::value > 1 && p.num_items > sms) ? 2 : 1;
+    int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(want, smem_sm, smem_blk);
+    if (stages == 0) stages = pick_stages<C>(1, smem_sm, smem_blk);
     if (stages == 0) return cudaErrorInvalidConfiguration;
     const size_t smem = make_layout<C>(stages).total;
     if ((int)smem > smem_blk) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
     int occ = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, smem)) != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
+    CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    if (C::TC) {
+        const long long rows = (long long)p.num_pages * p.Hkv * p.Ps;
+        if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
+        if ((e = make_cache_map(&tk, p.k, rows, D, p.Ps)) != cudaSuccess) return e;
+        if ((e = make_cache_map(&tv, p.v, rows, D, p.Ps)) != cudaSuccess) return e;
+    }
     p.stages = stages;
     int grid = sms * occ;
     if (grid > p.num_items) grid = p.num_items;
     if (li) { li->grid = grid; li->stages = stages; li->smem = smem; li->ctas_per_sm = occ; }
-    kern<<<grid, kThreads, smem, stream>>>(p);
+    kern<<<grid, C::THREADS, smem, stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 
