@@ -143,6 +143,34 @@ int dense_decode(const void* q, const void* k_cache, const void* v_cache,
                  const int32_t* visit_order, void* out, const art_shape* shape,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * art_decode without a caller-provided workspace. (An addition of this
+ * library; the ART paper has no counterpart.)
+ *
+ * Some callers cannot allocate device memory: for example a plug-in running
+ * inside a host framework that owns every device allocation through its own
+ * pool, or a decode loop whose latency budget rules out allocator calls. This
+ * entry point takes the same arguments as art_decode except the workspace,
+ * and keeps its scratch (the 64-byte header, per-item {n, flags} and the
+ * claim order) in a device array compiled into the library: 196,864 bytes per
+ * device that loads the library, held until the process exits. It calls no
+ * device allocator.
+ *   Limit: batch * num_kv_heads <= 16384; larger calls return
+ *          ART_ERR_UNSUPPORTED without touching the device.
+ *   Set-up: a device's first call looks up the array's device address
+ *          (cudaGetSymbolAddress) with that device current; make that first
+ *          call before any stream capture.
+ *   Sharing: every call on a device uses the same array. Each call clears
+ *          what must start at zero on `stream`, but calls that overlap on the
+ *          GPU (other streams, other threads) race on it and must be ordered
+ *          by the caller. art_read_device_status cannot read this array.
+ */
+int art_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* seq_lens,
+                      const int32_t* visit_order, float eps_mag, float eps_dir,
+                      int32_t patience, const int32_t* probe_idx, void* out,
+                      int32_t* blocks_used, const art_shape* shape, void* stream);
+
 /* Copies the device status word out of `workspace` (a blocking copy; call it
  * after the stream has finished the call of interest). Returns ART_OK or
  * ART_ERR_INVALID_ARG / ART_ERR_LAUNCH. */

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "art_common.cuh"
@@ -316,3 +317,57 @@ const char* art_status_string(int code) {
 const char* art_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// art_decode_static: art_decode with its workspace in a device array that
+// lives inside this library, for callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+namespace art {
+
+constexpr int kStaticMaxItems = 16384;  // largest batch * num_kv_heads accepted
+constexpr size_t kStaticWorkspaceBytes =
+    (sizeof(WsHeader) + (size_t)kStaticMaxItems * (sizeof(int32_t) + sizeof(ItemInfo)) + 255) / 256 * 256;
+
+// One copy per device that loads this library, kept until the process exits.
+// In host code this name only stands for the device array; its device address
+// comes from cudaGetSymbolAddress (below).
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+constexpr int kStaticMaxDevices = 256;
+static void* g_static_workspace_addr[kStaticMaxDevices];
+static std::mutex g_static_mutex;
+
+// Device address of g_static_workspace on the current device; looked up once
+// per device, on that device's first call.
+static int static_workspace(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kStaticMaxDevices) return ART_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_workspace_addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (!ptr) return ART_ERR_LAUNCH;
+        g_static_workspace_addr[dev] = ptr;
+    }
+    *out = g_static_workspace_addr[dev];
+    return ART_OK;
+}
+
+}  // namespace art
+
+extern "C" int art_decode_static(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                 const int32_t* seq_lens, const int32_t* visit_order, float eps_mag, float eps_dir,
+                                 int32_t patience, const int32_t* probe_idx, void* out, int32_t* blocks_used,
+                                 const art_shape* shape, void* stream) {
+    const int rc = check_shape(shape);
+    if (rc != ART_OK) return rc;
+    if ((long long)shape->batch * shape->num_kv_heads > kStaticMaxItems) return ART_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    const int rs = static_workspace(&ws);
+    if (rs != ART_OK) return rs;
+    return run<true>(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience, probe_idx,
+                     out, blocks_used, shape, ws, kStaticWorkspaceBytes, stream, nullptr);
+}
