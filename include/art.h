@@ -102,6 +102,7 @@ enum {
     ART_STATUS_BAD_SEQLEN = 8,  /* seq_len < 0 or beyond the block table             */
     ART_STATUS_BAD_PROBE = 16,  /* probe index out of range or repeated              */
     ART_STATUS_TIMEOUT = 32,    /* a bounded wait inside the kernel gave up          */
+    ART_STATUS_INTERNAL = 64,   /* an internal consistency check failed (the access was skipped) */
 };
 
 /* Bytes of device workspace art_decode / dense_decode need for `shape`.

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(HERE, "libart.so")
 ART_DTYPE_BF16, ART_DTYPE_F32 = 0, 1
 ART_OK, ART_ERR_INVALID_ARG, ART_ERR_UNSUPPORTED, ART_ERR_WORKSPACE, ART_ERR_LAUNCH = 0, -1, -2, -3, -4
 STATUS_BITS = {1: "bad visit entry", 2: "duplicate visit entry", 4: "bad page id", 8: "bad seq_len",
-               16: "bad probe index", 32: "wait timeout"}
+               16: "bad probe index", 32: "wait timeout", 64: "internal check failed"}
 EXPORTS = ("art_workspace_bytes", "art_decode", "dense_decode", "art_read_device_status",
            "art_status_string", "art_last_cuda_error")
 

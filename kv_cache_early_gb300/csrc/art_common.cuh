@@ -21,14 +21,29 @@ constexpr int kItemHas0 = 1;     // logical block 0 is in the visit list
 constexpr int kItemBad = 2;      // the item's device data failed a check
 
 // Slot kinds written by the producer into the ring metadata.
-enum SlotKind : int { kSlotBlock = 0, kSlotEmpty = 1, kSlotFail = 2, kSlotEnd = 3 };
+// kSlotPad: an entry without data that gives the second consumer group its
+// share of a one-block item.
+enum SlotKind : int { kSlotBlock = 0, kSlotEmpty = 1, kSlotFail = 2, kSlotEnd = 3, kSlotPad = 4 };
 
 struct WsHeader {
     unsigned int claim;      // next position of `order` to hand out
     unsigned int plan_done;  // plan CTAs that have finished
     int status;              // ART_STATUS_* bits
-    int pad[13];
+    int check_code;          // first failed internal check (0 = none)
+    int check_info[4];       // its details
+    int pad[8];
 };
+
+// Records the first failed internal consistency check (ART_STATUS_INTERNAL).
+__device__ __forceinline__ void record_check(WsHeader* hdr, int code, int a, int b, int c) {
+    if (atomicCAS(&hdr->check_code, 0, code) == 0) {
+        hdr->check_info[0] = a;
+        hdr->check_info[1] = b;
+        hdr->check_info[2] = c;
+        hdr->check_info[3] = (int)blockIdx.x;
+    }
+    atomicOr(&hdr->status, ART_STATUS_INTERNAL);
+}
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
 struct ItemInfo {
@@ -133,8 +148,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Named barrier among the consumer warps only (ids 1..15; 0 is __syncthreads).
+// Named barrier among a set of consumer warps (ids 1..15; 0 is __syncthreads).
+// bar.sync is a warp-aligned instruction: the warp is reconverged first.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 

@@ -40,6 +40,7 @@
 // the CTA returns.
 #pragma once
 
+#include <cstdlib>
 #include <cstring>
 
 #include "art_common.cuh"
@@ -56,11 +57,16 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 
 enum Decision : int { kContinue = 0, kStop = 1, kDiscard = 2 };
 
-template <bool kBF16, int D, int G>
+template <bool kBF16, int D, int G, int kNG = 1>
 struct Cfg {
     using E = Elem<kBF16>;
     static constexpr bool TC = kBF16;            // bf16: tensor-core consumers on swizzled tiles
-    static constexpr int NWC = TC ? 4 : 8;       // consumer warps
+    static constexpr int NG = TC ? kNG : 1;      // consumer groups (alternate ring entries of one item)
+    static constexpr int GW = TC ? 4 : 8;        // warps per consumer group
+    static constexpr int NWC = NG * GW;          // consumer warps
+    // record buffers: a group publishes entry u after the decision on u - 2 NG, which the
+    // statistics warp may send before it has read u - 2 NG's partials
+    static constexpr int NB = TC ? 4 * NG : 2;
     static constexpr int THREADS = (NWC + 2) * 32;
     static constexpr int GQ = G;                 // query heads per KV head
     static constexpr int ELT = E::kBytes;
@@ -71,7 +77,7 @@ struct Cfg {
     static constexpr int E2 = EPC / 2;           // packed pairs per chunk
     static constexpr int LPR = ROWB / CB;        // lanes covering one row
     static constexpr int RPW = 32 / LPR;         // rows per warp instruction
-    static constexpr int RW = kBK / NWC;         // rows per consumer warp per block
+    static constexpr int RW = kBK / GW;          // rows per consumer warp per block
     static constexpr int NI = RW / RPW;          // warp instructions per block
     static constexpr int NV = NI * G;            // partial scores per lane
     static constexpr int NVP = pow2ceil(imax(NV, LPR));
@@ -80,7 +86,7 @@ struct Cfg {
     static constexpr int SLOT = (int)align_up((size_t)2 * KVB + QB, TC ? 1024 : 16);
     static constexpr int SPL = (G * kMaxProbe + 31) / 32;  // probe slots per stat lane
     static constexpr int PRW = TC ? 1 : RPW;     // probe partial rows per warp
-    static constexpr int PART_F = 2 * NWC * PRW * G * kMaxProbe;
+    static constexpr int PART_F = NB * GW * PRW * G * kMaxProbe;
     static constexpr int KS = D / 16;            // tensor-core k-steps (QK) and m-tiles (PV)
     static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
     static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
@@ -94,10 +100,11 @@ struct SlotMeta {
 };
 
 struct Ctrl {
-    int dec[2];
+    int dec[8];
     int stop_item;
     int abort;
-    SlotMeta info[2];  // item and position of each published partial
+    int pad0, pad1;
+    SlotMeta info[8];  // item and position of each published record
 };
 
 struct Layout {
@@ -113,24 +120,24 @@ __host__ __device__ inline Layout make_layout(int stages) {
     o += (size_t)stages * sizeof(SlotMeta);
     o = align_up(o, 16);
     L.bars = o;
-    o += (size_t)(2 * stages + 5) * sizeof(uint64_t);
+    o += (size_t)(2 * stages + 2 * C::NB + 1) * sizeof(uint64_t);
     o = align_up(o, 16);
     L.part = o;  // [2][NWC][RPW][G][kMaxProbe] probe partials
     o += (size_t)C::PART_F * sizeof(float);
-    L.plb = o;  // [2][NWC][G] per-warp block sums
-    o += (size_t)2 * C::NWC * G * sizeof(float);
-    L.pmb = o;  // [2][G] block maxima
-    o += (size_t)2 * G * sizeof(float);
+    L.plb = o;  // [NB][GW][G] per-warp block sums
+    o += (size_t)C::NB * C::GW * G * sizeof(float);
+    L.pmb = o;  // [NB][G] block maxima
+    o += (size_t)C::NB * G * sizeof(float);
     L.wmax = o;  // [2][NWC][8] per-warp maxima of the block being processed (by block parity)
     o += (size_t)2 * C::NWC * 8 * sizeof(float);
     L.scr = o;  // [NWC][G][RW] scores, then weights
     o += (size_t)C::NWC * G * C::RW * sizeof(float);
     o = align_up(o, 16);
-    L.eacc = o;  // per consumer warp: [G][D] output sums, then [G] weight sums
-    o += (size_t)C::NWC * (G * C::DD + G) * sizeof(float);
+    L.eacc = o;  // per consumer warp: [G][D] output sums, then [G] weight sums, then [G] maxima
+    o += (size_t)C::NWC * (G * C::DD + 2 * G) * sizeof(float);
     o = align_up(o, 1024);
-    L.qt = o;  // tensor-core path: the item's queries, 8 rows (heads past G zero), 128B-swizzled
-    o += C::TC ? (size_t)8 * C::ROWB : 0;
+    L.qt = o;  // tensor-core path, per group: the item's queries, 8 rows (heads past G zero), 128B-swizzled
+    o += C::TC ? (size_t)C::NG * 8 * C::ROWB : 0;
     o = align_up(o, 16);
     L.sh = o;  // [3][G] statistics warp scratch
     o += (size_t)3 * G * sizeof(float);
@@ -174,21 +181,26 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // Waits for the phase with `parity` of `bar` to complete, warp-uniformly. The
 // threads sleep in mbarrier.try_wait (woken by the phase completing) rather
-// than spin. Returns false when the CTA is aborting or the wait exceeded
-// kWaitLimitNs.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctrl* ctrl, WsHeader* hdr) {
+// than spin. Returns false (and sets ART_STATUS_TIMEOUT) when the wait exceeds
+// kWaitLimitNs. Only a warp's own wait ends it: the warps of a consumer group
+// always wait on the same barrier phases, so they give up together and none is
+// left behind in a named barrier.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctrl* ctrl, WsHeader* hdr,
+                                             int where = 0) {
     constexpr uint32_t kSleepNs = 200000;  // upper bound of one sleep; the limit is checked between sleeps
     if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
-        int stop = ld_volatile_shared(&ctrl->abort);
-        if (!stop && (threadIdx.x & 31) == 0 && global_ns() - t0 > kWaitLimitNs) {
-            st_volatile_shared(&ctrl->abort, 1);
-            atomicOr(&hdr->status, ART_STATUS_TIMEOUT);
-            stop = 1;
+        int late = (threadIdx.x & 31) == 0 && global_ns() - t0 > kWaitLimitNs;
+        if (__any_sync(0xffffffffu, late)) {
+            if ((threadIdx.x & 31) == 0) {
+                st_volatile_shared(&ctrl->abort, 1);
+                atomicOr(&hdr->status, ART_STATUS_TIMEOUT);
+                if (where) record_check(hdr, where, (int)parity, (int)(threadIdx.x >> 5), 0);
+            }
+            return false;
         }
-        if (__any_sync(0xffffffffu, stop)) return false;
     }
 }
 
@@ -208,7 +220,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
 
     auto acquire = [&]() -> bool {
         if (have_slot) return true;
-        if (!wait_bounded(&empty[slot], (round & 1u) ^ 1u, ctrl, p.hdr)) return false;
+        if (!wait_bounded(&empty[slot], (round & 1u) ^ 1u, ctrl, p.hdr, 131)) return false;
         have_slot = true;
         return true;
     };
@@ -220,16 +232,22 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
             ++round;
         }
     };
-    auto emit = [&](int kind, int item, int b, int g) -> bool {
+    // an entry without data; every consumer group gets one (kind, item) entry
+    auto emit1 = [&](int kind, int item, int b, int g, int pos, int n) -> bool {
         if (!acquire()) return false;
         if (lane == 0) {
             SlotMeta& mt = meta[slot];
-            mt.item = item; mt.pos = 0; mt.n = 0; mt.c = 0; mt.nvalid = 0; mt.kind = kind;
+            mt.item = item; mt.pos = pos; mt.n = n; mt.c = -1; mt.nvalid = 0; mt.kind = kind;
             mt.b = b; mt.g = g; mt.has0 = 0;
             mbar_arrive(&full[slot]);
         }
         __syncwarp();
         advance();
+        return true;
+    };
+    auto emit = [&](int kind, int item, int b, int g) -> bool {
+        for (int k = 0; k < C::NG; ++k)
+            if (!emit1(kind, item, b, g, k, 0)) return false;
         return true;
     };
 
@@ -242,6 +260,11 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
             break;
         }
         const int item = __ldg(&p.order[idx]);
+        if (item < 0 || item >= p.num_items) {
+            if (lane == 0) record_check(p.hdr, 1, idx, item, 0);
+            ok = emit(kSlotEnd, -1, 0, 0);
+            break;
+        }
         const ItemInfo inf = p.info[item];
         const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
         if (inf.flags & kItemBad) {
@@ -309,7 +332,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                     break;
                 }
                 const int posj = base + j;
-                const bool with_q = (posj == 0);
+                const bool with_q = posj < C::NG;  // each consumer group's first entry of the item
                 const uint32_t page_bytes = (uint32_t)((p.Ps <= kBK ? p.Ps : kBK) * C::ROWB);
                 const uint32_t bytes = 2u * npj * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
                 unsigned char* dst = ring + (size_t)slot * C::SLOT;
@@ -368,6 +391,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
             if (!ok) break;
         }
         if (!ok) break;
+        if (C::NG > 1 && n == 1 && !(ok = emit1(kSlotPad, item, b, g, 1, 1))) break;
     }
 
     if (!ok) {
@@ -392,7 +416,9 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
                           uint64_t* part_full, uint64_t* dec_bar, Ctrl* ctrl) {
     constexpr int G = C::GQ;
     constexpr int SPL = C::SPL;
-    constexpr int NP = C::NWC * C::PRW;  // partial rows per probe slot
+    constexpr int NP = C::GW * C::PRW;  // partial rows per probe slot
+    constexpr int NB = C::NB;
+    (void)sh;
     const int lane = threadIdx.x & 31;
     const int m = p.m;
     const int GM = G * m;
@@ -404,108 +430,128 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         hs[j] = k < GM ? k / m : -1;
         off[j] = k < GM ? (k / m) * kMaxProbe + (k - (k / m) * m) : 0;
     }
-    float Mh = -INFINITY, Lh = 0.f;  // running max / sum of head `lane` (lanes < G)
+    float M[G], Lsum[G];  // running max / sum per head (every lane keeps all heads)
     float X[SPL];
-    float n2prev = 0.f;               // |x_{i-1}|^2
+    float nprev = 0.f;  // |x_{i-1}|
     int counter = 0, seen0 = 0;
     int stopped_item = -1;
     auto reset = [&]() {
-        Mh = -INFINITY;
-        Lh = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) { M[h] = -INFINITY; Lsum[h] = 0.f; }
 #pragma unroll
         for (int j = 0; j < SPL; ++j) X[j] = 0.f;
-        n2prev = 0.f;
+        nprev = 0.f;
         counter = 0;
         seen0 = 0;
     };
-    reset();
-    for (int v = 0;; ++v) {
-        const int vb = v & 1;
-        if (!wait_bounded(&part_full[vb], (uint32_t)(v >> 1) & 1u, ctrl, p.hdr)) return;
-        const SlotMeta* info = &ctrl->info[vb];
-        const int kind = info->kind, item = info->item;
-        int dec = kStop;
-        if (kind == kSlotEnd) return;
-        if (kind != kSlotBlock) {
-            if (lane == 0) p.blocks_used[item] = kind == kSlotFail ? -1 : 0;
-            reset();
-        } else if (item == stopped_item) {
-            dec = kDiscard;  // computed ahead of the decision that stopped its item
-        } else {
-            const int pos = info->pos, n = info->n, c = info->c, has0 = info->has0;
-            if (pos == 0) reset();
-            // per head (lane h < G): block sum, new running max and sum; the probe of
-            // head h moves by delta = coef_h * (PV_probe - l_blk,h * x)
-            if (lane < G) {
-                const float mb = pmb[vb * G + lane];
-                float lb = 0.f;
-#pragma unroll
-                for (int w = 0; w < C::NWC; ++w) lb += plb[(vb * C::NWC + w) * G + lane];
-                const float Mn = fmaxf(Mh, mb);
-                const float a = exp2f(Mh - Mn);
-                const float bw = exp2f(mb - Mn);
-                const float Ln = a * Lh + bw * lb;
-                sh[lane] = bw / Ln;
-                sh[G + lane] = lb;
-                Mh = Mn;
-                Lh = Ln;
-            }
-            __syncwarp();
-            const float* pp = part + (size_t)vb * NP * G * kMaxProbe;
-            float s1 = 0.f, s2 = 0.f, s3 = 0.f;  // sum delta^2, sum delta . x_{i-1}, |x_i|^2
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) {
-                const int h = hs[j];
-                if (h >= 0) {
-                    float pb = 0.f;
-#pragma unroll
-                    for (int w = 0; w < NP; ++w) pb += pp[w * G * kMaxProbe + off[j]];
-                    const float d = sh[h] * (pb - sh[G + h] * X[j]);
-                    s1 = fmaf(d, d, s1);
-                    s2 = fmaf(d, X[j], s2);
-                    X[j] += d;
-                    s3 = fmaf(X[j], X[j], s3);
-                }
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-                s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-                s3 += __shfl_xor_sync(0xffffffffu, s3, o);
-            }
-            // |x_i| - |x_{i-1}| = (|x_i|^2 - |x_{i-1}|^2) / (|x_i| + |x_{i-1}|) with the
-            // difference of squares formed directly as 2 s2 + s1;
-            // 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2 = (s1 - 2 s2 dn / n_{i-1} + dn^2) / (2 |x_i|^2)
-            const float nprev = sqrtf(n2prev);
-            const float g2 = 2.f * s2 + s1;
-            const float n2 = s3;
-            const float ni = sqrtf(n2);
-            bool stable = false;
-            if (pos >= 1) {
-                const float dn = g2 / (ni + nprev);
-                const float dmag = fabsf(dn) / nprev;
-                const float ddir = fmaxf(0.f, (s1 - 2.f * s2 * (dn / nprev) + dn * dn) / (2.f * n2));
-                stable = nprev > 0.f && ni > 0.f && isfinite(nprev) && isfinite(ni) && isfinite(dmag) &&
-                         isfinite(ddir) && dmag < p.eps_mag && ddir < p.eps_dir;
-            }
-            n2prev = n2;
-            counter = stable ? counter + 1 : 0;
-            if (c == 0) seen0 = 1;
-            const bool stop = ((counter >= p.patience) && (seen0 || !has0)) || (pos == n - 1);
-            dec = stop ? kStop : kContinue;
-            if (stop) {
-                stopped_item = item;
-                if (lane == 0) {
-                    p.blocks_used[item] = pos + 1;
-                    st_volatile_shared(&ctrl->stop_item, item);
-                }
-            }
-        }
+    auto send = [&](int vb, int dec) {
+        __syncwarp();
         if (lane == 0) {
             ctrl->dec[vb] = dec;
             mbar_arrive(&dec_bar[vb]);
         }
-        __syncwarp();
+    };
+    reset();
+    for (int v = 0;; ++v) {
+        const int vb = v % NB;
+        if (!wait_bounded(&part_full[vb], (uint32_t)(v / NB) & 1u, ctrl, p.hdr, 141)) return;
+        const SlotMeta* info = &ctrl->info[vb];
+        const int kind = info->kind, item = info->item;
+        if (kind == kSlotEnd) return;
+        if (item == stopped_item || kind == kSlotPad) {
+            // computed ahead of the decision that stopped its item, a pad, or the
+            // second group's copy of a failed / empty item
+            send(vb, kDiscard);
+            continue;
+        }
+        if (kind != kSlotBlock) {
+            if (lane == 0) p.blocks_used[item] = kind == kSlotFail ? -1 : 0;
+            reset();
+            stopped_item = item;
+            send(vb, kStop);
+            continue;
+        }
+        const int pos = info->pos, n = info->n, c = info->c, has0 = info->has0;
+        if (pos == 0) reset();
+        if (c == 0) seen0 = 1;
+        // the stop can only happen here if the patience count can reach p at this
+        // block and block 0 (when listed) has been processed; otherwise the
+        // consumers learn "continue" at once and the statistics follow
+        const bool last = pos == n - 1;
+        const bool may_stop = (counter + 1 >= p.patience) && (seen0 || !has0);
+        bool sent = false;
+        if (last || !may_stop) {
+            send(vb, last ? kStop : kContinue);
+            sent = true;
+        }
+        // per head: block sum over the warps, new running max and sum, and the
+        // factor that moves the probe: delta = coef_h * (PV_probe - l_blk,h * x)
+        float coef[G], lbh[G];
+        const float* pp = part + (size_t)vb * NP * G * kMaxProbe;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float mb = pmb[vb * G + h];
+            float lb = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::GW; ++w) lb += plb[(vb * C::GW + w) * G + h];
+            const float Mn = fmaxf(M[h], mb);
+            const float a = exp2f(M[h] - Mn);
+            const float bw = exp2f(mb - Mn);
+            const float Ln = a * Lsum[h] + bw * lb;
+            coef[h] = bw / Ln;
+            lbh[h] = lb;
+            M[h] = Mn;
+            Lsum[h] = Ln;
+        }
+        float s1 = 0.f, s2 = 0.f, s3 = 0.f;  // sum delta^2, sum delta . x_{i-1}, |x_i|^2
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) {
+            const int h = hs[j];
+            if (h >= 0) {
+                float pb = 0.f;
+#pragma unroll
+                for (int w = 0; w < NP; ++w) pb += pp[w * G * kMaxProbe + off[j]];
+                float cf = 0.f, lb = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+                    if (hh == h) { cf = coef[hh]; lb = lbh[hh]; }
+                const float d = cf * (pb - lb * X[j]);
+                s1 = fmaf(d, d, s1);
+                s2 = fmaf(d, X[j], s2);
+                X[j] += d;
+                s3 = fmaf(X[j], X[j], s3);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+            s3 += __shfl_xor_sync(0xffffffffu, s3, o);
+        }
+        // |x_i| - |x_{i-1}| = (|x_i|^2 - |x_{i-1}|^2) / (|x_i| + |x_{i-1}|) with the
+        // difference of squares formed directly as 2 s2 + s1;
+        // 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2 = (s1 - 2 s2 dn / n_{i-1} + dn^2) / (2 |x_i|^2)
+        const float ni = sqrtf(s3);
+        bool stable = false;
+        if (pos >= 1) {
+            const float dn = (2.f * s2 + s1) / (ni + nprev);
+            const float rprev = 1.f / nprev;
+            const float dmag = fabsf(dn) * rprev;
+            const float ddir = fmaxf(0.f, (s1 - 2.f * s2 * (dn * rprev) + dn * dn) / (2.f * s3));
+            stable = nprev > 0.f && ni > 0.f && isfinite(nprev) && isfinite(ni) && isfinite(dmag) &&
+                     isfinite(ddir) && dmag < p.eps_mag && ddir < p.eps_dir;
+        }
+        nprev = ni;
+        counter = stable ? counter + 1 : 0;
+        const bool stop = last || (may_stop && counter >= p.patience);
+        if (stop) {
+            stopped_item = item;
+            if (lane == 0) {
+                p.blocks_used[item] = pos + 1;
+                st_volatile_shared(&ctrl->stop_item, item);
+            }
+        }
+        if (!sent) send(vb, stop ? kStop : kContinue);
     }
 }
 
@@ -625,7 +671,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
             for (int h = 0; h < G; ++h)
 #pragma unroll
                 for (int e = 0; e < EPC; ++e) fa[h][e] += __shfl_xor_sync(0xffffffffu, fa[h][e], s);
-        float* mine = eacc + (size_t)w * (G * D + G);  // this warp's [G][D] sums, then [G] weights
+        float* mine = eacc + (size_t)w * (G * D + 2 * G);  // this warp's [G][D] sums, then [G] weights
         if (half == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h)
@@ -645,8 +691,8 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
             float num = 0.f, den = 0.f;
 #pragma unroll
             for (int ww = 0; ww < kNWC; ++ww) {
-                num += eacc[(size_t)ww * (G * D + G) + idx];
-                den += eacc[(size_t)ww * (G * D + G) + G * D + h];
+                num += eacc[(size_t)ww * (G * D + 2 * G) + idx];
+                den += eacc[(size_t)ww * (G * D + 2 * G) + G * D + h];
             }
             E::store(p.out, out_index(b, g, h, col), num / den);
         }
@@ -888,22 +934,35 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
 
 
 // ---------------------------------------------------------------------------
-// tensor-core consumer warps (bf16). Warp w owns keys 16w .. 16w+15 of the
-// block. S^T (16 keys x 8 heads) = K (16 x d) . Q^T (d x 8) with
-// mma.m16n8k16, K fragments by ldmatrix from the 128B-swizzled tile; the
-// weights are split into bf16 hi + lo parts (p = hi + lo to ~2^-17) and
+// tensor-core consumer warps (bf16), in NG groups of GW warps. Group k takes
+// ring entries u = k, k + NG, ... of the same stream of items, so NG blocks of
+// one item are in flight at once; each group keeps its own partial
+// accumulators, and when an item ends the groups merge them together.
+//
+// Warp wg of a group owns keys 16 wg .. 16 wg + 15 of a block.
+// S^T (16 keys x 8 heads) = K (16 x d) . Q^T (d x 8) with mma.m16n8k16, K and
+// Q^T fragments by ldmatrix from 128B-swizzled tiles; the weights are split
+// into bf16 hi + lo parts (p = hi + lo to ~2^-17) and
 // O^T (d x 8 heads) += V^T (d x 16 keys) . P^T (16 keys x 8 heads), V^T
 // fragments by ldmatrix.trans, P^T fragments by movmatrix of the S^T layout.
 // Heads beyond G are carried as zeros.
+//
+// Every entry gives the statistics warp one record (a computed block, or a
+// block / pad / failed / empty entry without data), in entry order. A group
+// publishes the record of its current entry, then waits for the decision on
+// its previous entry: "continue" folds that block into the group's
+// accumulators, "stop" folds it and ends the item, "discard" (a block past a
+// stop) ends the item without folding. A group also ends its item when its
+// next entry belongs to another item.
 // ---------------------------------------------------------------------------
 template <class C, bool kART>
 __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta* meta, uint64_t* full,
                             uint64_t* empty, uint64_t* part_full, uint64_t* dec_bar, uint64_t* cbar, const Layout& L,
                             unsigned char* smem, const int* prank, Ctrl* ctrl) {
-    constexpr int G = C::GQ, D = C::DD, KS = C::KS, NWC = C::NWC;
-    constexpr bool LAG = kART && C::LAG;
+    constexpr int G = C::GQ, D = C::DD, KS = C::KS, NWC = C::NWC, GW = C::GW, NG = C::NG, NB = C::NB;
     using E = typename C::E;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = w / GW, wg = w % GW;  // group, warp within the group
     const int grp = lane >> 2, tig = lane & 3;
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
     const bool v0 = h0 < G, v1 = h1 < G;
@@ -912,8 +971,12 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
     float* pmb = reinterpret_cast<float*>(smem + L.pmb);
     float* wmax = reinterpret_cast<float*>(smem + L.wmax);
     float* eacc = reinterpret_cast<float*>(smem + L.eacc);
+    unsigned char* sQt = smem + L.qt + (size_t)gi * 8 * C::ROWB;
+    const uint32_t qtbase = smem_addr(sQt);
     const float scale = 1.4426950408889634f / sqrtf((float)D);
-    const int ctid = threadIdx.x;
+    const int ctid = threadIdx.x;   // 0 .. NWC*32-1
+    const int gtid = ctid % (GW * 32);
+    const int gbar = 1 + gi;        // named barrier of the group
     // this lane's O^T rows are d = 16 mt + grp + 8 r; bit 2 mt + r marks a probe column,
     // byte 2 mt + r of prk holds its rank among the probe columns
     uint32_t pbits = 0;
@@ -933,21 +996,16 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
             }
     }
     const int mi = lane >> 3, lr = lane & 7;
-    const int keyK = w * 16 + (mi & 1) * 8 + lr;   // K rows for the S^T A fragments
+    const int keyK = wg * 16 + (mi & 1) * 8 + lr;   // K rows for the S^T A fragments
     const int chK = mi >> 1;
-    const int keyV = w * 16 + (mi >> 1) * 8 + lr;  // V rows for the O^T A fragments
+    const int keyV = wg * 16 + (mi >> 1) * 8 + lr;  // V rows for the O^T A fragments
     const int chV = mi & 1;
     auto sw = [](uint32_t base, int row, int chunk) -> uint32_t {
         return base + (uint32_t)((chunk >> 3) * (kBK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
     };
 
     float acc[KS][4], tN[KS][4], tP[KS][4];
-    unsigned char* sQt = smem + L.qt;
-    const uint32_t qtbase = smem_addr(sQt);
     float mrun[2], lrun[2], mbN[2], lbN[2], mbP[2], lbP[2];
-    int itemP = -1, bP = 0, gP = 0;  // item of the pending block
-    int vP = 0;
-    bool pending = false;
     auto reset = [&]() {
 #pragma unroll
         for (int j = 0; j < 2; ++j) { mrun[j] = -INFINITY; lrun[j] = 0.f; }
@@ -963,49 +1021,33 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
         for (int c = 0; c < 4; ++c) tN[mt][c] = tP[mt][c] = 0.f;
     mbN[0] = mbN[1] = mbP[0] = mbP[1] = lbN[0] = lbN[1] = lbP[0] = lbP[1] = 0.f;
 
-    int slot = 0;
-    uint32_t round = 0;
-    int v = 0;
-    uint32_t cbph = 0;
-    int bpar = 0;
-    int stopped_item = -1;
+    int u = gi;            // this group's current ring entry (= its record number)
+    int bpar = 0;          // parity of the blocks this group computed (wmax buffer)
+    uint32_t cbph = 0;     // phase of the all-consumer barrier
+    int cur_item = -1, curb = 0, curg = 0;  // the item held in this group's accumulators
+    int stopped_item = -1;                  // the last item this group ended
+    bool pending = false, pcomp = false;    // previous entry awaiting its decision; computed?
+    int uP = 0, itemP = -1, posP = 0, nP = 0;
 
     auto cbar_sync = [&]() -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(cbar);
-        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr);
+        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr, 111 + gi);
         cbph ^= 1u;
         return r;
-    };
-    auto release = [&]() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-    };
-    auto advance = [&]() {
-        if (++slot == p.stages) { slot = 0; ++round; }
     };
     auto out_index = [&](int b, int g, int h, int col) -> size_t {
         return ((size_t)b * p.Hq + (size_t)g * G + h) * D + col;
     };
-    auto publish = [&](const SlotMeta& mt) -> int {
-        const int vb = v & 1;
-        if (w == 0 && lane == 0) {
-            SlotMeta& r = ctrl->info[vb];
-            r.kind = mt.kind; r.item = mt.item; r.pos = mt.pos; r.n = mt.n; r.c = mt.c; r.has0 = mt.has0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&part_full[vb]);
-        return v++;
-    };
     auto wait_dec = [&](int rec) -> int {
-        if (!wait_bounded(&dec_bar[rec & 1], (uint32_t)(rec >> 1) & 1u, ctrl, p.hdr)) return -1;
-        return ctrl->dec[rec & 1];
+        if (!wait_bounded(&dec_bar[rec % NB], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 121 + gi)) return -1;
+        return ctrl->dec[rec % NB];
     };
     auto fold = [&](const float (&t)[KS][4], const float* mb, const float* lb) {
         float a[2], bb[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            if (mb[j] == -INFINITY) {  // a head beyond G
+            if (mb[j] == -INFINITY) {  // a head beyond G, or no valid key
                 a[j] = 1.f;
                 bb[j] = 0.f;
                 continue;
@@ -1021,8 +1063,10 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[mt][c] = a[c & 1] * acc[mt][c] + bb[c & 1] * t[mt][c];
     };
-    auto epilogue = [&](int b, int g) -> bool {
-        float* mine = eacc + (size_t)w * (G * D + G);
+    // both groups together: merge the per-warp partials of the item (each group
+    // has its own running maxima) and write O = sum / weight sum
+    auto finalize = [&]() -> bool {
+        float* mine = eacc + (size_t)w * (G * D + 2 * G);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
@@ -1032,171 +1076,44 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
                 if (v1) mine[h1 * D + d] = acc[mt][2 * r + 1];
             }
         if (grp == 0) {
-            if (v0) mine[G * D + h0] = lrun[0];
-            if (v1) mine[G * D + h1] = lrun[1];
+            if (v0) { mine[G * D + h0] = lrun[0]; mine[G * D + G + h0] = mrun[0]; }
+            if (v1) { mine[G * D + h1] = lrun[1]; mine[G * D + G + h1] = mrun[1]; }
         }
         if (!cbar_sync()) return false;
+        const int ob = curb, og = curg;  // both groups hold the same item
+        const bool okbg = ob >= 0 && ob < p.B && og >= 0 && og < p.Hkv;
+        if (!okbg && ctid == 0) record_check(p.hdr, 3, ob, og, u);
         for (int idx = ctid; idx < G * D; idx += NWC * 32) {
-            const int h = idx / D, col = idx - (idx / D) * D;
+            const int h = idx / D;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int ww = 0; ww < NWC; ++ww) mx = fmaxf(mx, eacc[(size_t)ww * (G * D + 2 * G) + G * D + G + h]);
             float num = 0.f, den = 0.f;
 #pragma unroll
             for (int ww = 0; ww < NWC; ++ww) {
-                num += eacc[(size_t)ww * (G * D + G) + idx];
-                den += eacc[(size_t)ww * (G * D + G) + G * D + h];
+                const float* e = eacc + (size_t)ww * (G * D + 2 * G);
+                const float mw = e[G * D + G + h];
+                const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
+                num += f * e[idx];
+                den += f * e[G * D + h];
             }
-            E::store(p.out, out_index(b, g, h, col), num / den);
+            if (okbg) E::store(p.out, out_index(ob, og, h, idx - h * D), num / den);
         }
         return cbar_sync();
     };
     auto write_zero = [&](int b, int g) {
-        for (int idx = ctid; idx < G * D; idx += NWC * 32) E::store(p.out, out_index(b, g, idx / D, idx % D), 0.f);
-    };
-    auto resolve_pending = [&]() -> bool {
-        const int d = wait_dec(vP);
-        if (d < 0) return false;
-        fold(tP, mbP, lbP);
-        pending = false;
-        if (d == kStop) {
-            if (!epilogue(bP, gP)) return false;
-            reset();
-            stopped_item = itemP;
-        }
-        return true;
-    };
-
-    for (;;) {
-        if (!wait_bounded(&full[slot], round & 1u, ctrl, p.hdr)) return;
-        const SlotMeta mt = meta[slot];
-        if (mt.kind == kSlotEnd) {
-            if (LAG && pending && !resolve_pending()) return;
-            if (kART) publish(mt);
+        if (b < 0 || b >= p.B || g < 0 || g >= p.Hkv) {
+            if (gtid == 0) record_check(p.hdr, 4, b, g, u);
             return;
         }
-        if (mt.kind != kSlotBlock) {
-            release();
-            if (LAG && pending && !resolve_pending()) return;
-            if (mt.item != stopped_item) {
-                write_zero(mt.b, mt.g);
-                if (kART && wait_dec(publish(mt)) < 0) return;
-                reset();
-                stopped_item = mt.item;
-            }
-            advance();
-            continue;
-        }
-        if (mt.item == stopped_item) {
-            release();
-            advance();
-            continue;
-        }
-        unsigned char* sK = ring + (size_t)slot * C::SLOT;
-        unsigned char* sV = sK + C::KVB;
-        if (mt.pos == 0) {
-            // the item's queries into the swizzled 8-row area (rows past G zero); every warp
-            // has finished the previous item's scores before the barrier of its last block
-            const unsigned char* sQ = sK + 2 * C::KVB;
-            constexpr int QCH = 8 * (C::ROWB / 16);
-            for (int i = ctid; i < QCH; i += NWC * 32) {
-                const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
-                const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
-            }
-            named_bar_sync(1, NWC * 32);
-        }
-        const int nvalid = mt.nvalid;
-
-        // ---- S^T for this warp's 16 keys
-        float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};  // two independent chains
-        const uint32_t kbase = smem_addr(sK), vbase = smem_addr(sV);
-#pragma unroll
-        for (int kp = 0; kp < KS / 2; ++kp) {
-            // B fragments (Q^T) of k-steps 2kp and 2kp+1: rows = heads, 8 columns each
-            uint32_t b00, b01, b10, b11;
-            {
-                const int c = 4 * kp + mi;
-                ldsm_x4(qtbase + (uint32_t)((c >> 3) * 1024 + lr * 128 + (((c & 7) ^ lr) << 4)), b00, b01, b10, b11);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int ks = 2 * kp + h;
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(sw(kbase, keyK, 2 * ks + chK), a0, a1, a2, a3);
-                mma_bf16(h ? s4b : s4, a0, a1, a2, a3, h ? b10 : b00, h ? b11 : b01);
-            }
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) s4[c] += s4b[c];
-        const int k0 = w * 16 + grp, k1 = k0 + 8;
-        float sc[4];
-        sc[0] = (k0 < nvalid && v0) ? s4[0] * scale : -INFINITY;
-        sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
-        sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
-        sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
-        // ---- block max per head: over this warp's keys, then across the warps
-        float m0 = fmaxf(sc[0], sc[2]), m1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
-            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-        }
-        if (grp == 0) {
-            wmax[(bpar * NWC + w) * 8 + h0] = m0;
-            wmax[(bpar * NWC + w) * 8 + h1] = m1;
-        }
-        named_bar_sync(1, NWC * 32);
-        float mb0 = -INFINITY, mb1 = -INFINITY;
-#pragma unroll
-        for (int ww = 0; ww < NWC; ++ww) {
-            mb0 = fmaxf(mb0, wmax[(bpar * NWC + ww) * 8 + h0]);
-            mb1 = fmaxf(mb1, wmax[(bpar * NWC + ww) * 8 + h1]);
-        }
-        bpar ^= 1;
-        float pw[4];
-        pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mb0);
-        pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mb1);
-        pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - mb0);
-        pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - mb1);
-        float l0 = pw[0] + pw[2], l1 = pw[1] + pw[3];
-#pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-        }
-        mbN[0] = mb0; mbN[1] = mb1; lbN[0] = l0; lbN[1] = l1;
-        // ---- P^T fragments: hi and lo bf16 parts, transposed by movmatrix
-        const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
-        const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
-        const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
-        const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB), bl0 = movm_t(lA), bl1 = movm_t(lB);
-        // ---- rows past the sequence end hold stale data: zero this warp's, so 0 * V stays 0
-        if (nvalid < w * 16 + 16) {
-            const int r0 = max(nvalid, w * 16);
-            const int nchunks = (w * 16 + 16 - r0) * (C::ROWB / 16);
-            for (int i = lane; i < nchunks; i += 32) {
-                const int row = r0 + i / (C::ROWB / 16), c = i % (C::ROWB / 16);
-                *reinterpret_cast<uint4*>(sV + (c >> 3) * (kBK * 128) + row * 128 + (c & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-        // ---- O^T partial of this block
-#pragma unroll
-        for (int m = 0; m < KS; ++m) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(sw(vbase, keyV, 2 * m + chV), a0, a1, a2, a3);
-            tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
-            mma_bf16(tN[m], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
-        }
-        release();
-
+        for (int idx = gtid; idx < G * D; idx += GW * 32) E::store(p.out, out_index(b, g, idx / D, idx % D), 0.f);
+    };
+    // the record of entry u for the statistics warp
+    auto publish = [&](const SlotMeta& mt, int kind, bool computed) {
+        const int rb = u % NB;
         if (kART) {
-            // probe partials of this block, then the record for the statistics warp
-            auto publish_block = [&]() -> int {
-                const int vb = v & 1;
-                float* pp = part + ((size_t)vb * NWC + w) * G * kMaxProbe;
+            if (computed) {
+                float* pp = part + ((size_t)rb * GW + wg) * G * kMaxProbe;
 #pragma unroll
                 for (int m = 0; m < KS; ++m)
 #pragma unroll
@@ -1207,76 +1124,204 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
                         if (on && v1) pp[h1 * kMaxProbe + rank] = tN[m][2 * r + 1];
                     }
                 if (grp == 0) {
-                    if (v0) plb[(vb * NWC + w) * G + h0] = l0;
-                    if (v1) plb[(vb * NWC + w) * G + h1] = l1;
-                    if (w == 0) {
-                        if (v0) pmb[vb * G + h0] = mb0;
-                        if (v1) pmb[vb * G + h1] = mb1;
+                    if (v0) plb[(rb * GW + wg) * G + h0] = lbN[0];
+                    if (v1) plb[(rb * GW + wg) * G + h1] = lbN[1];
+                    if (wg == 0) {
+                        if (v0) pmb[rb * G + h0] = mbN[0];
+                        if (v1) pmb[rb * G + h1] = mbN[1];
                     }
-                }
-                return publish(mt);
-            };
-            if (LAG) {
-                // the previous block's decision (computed during this block) decides it
-                if (pending) {
-                    const int d = wait_dec(vP);
-                    if (d < 0) return;
-                    fold(tP, mbP, lbP);
-                    pending = false;
-                    if (d == kStop) {
-                        if (!epilogue(bP, gP)) return;
-                        reset();
-                        stopped_item = itemP;
-                        if (mt.item == itemP) {  // computed past the stop: dropped, never published
-                            advance();
-                            continue;
-                        }
-                    }
-                }
-                const int vN = publish_block();
-#pragma unroll
-                for (int m = 0; m < KS; ++m)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) tP[m][c] = tN[m][c];
-                mbP[0] = mbN[0]; mbP[1] = mbN[1]; lbP[0] = lbN[0]; lbP[1] = lbN[1];
-                itemP = mt.item; bP = mt.b; gP = mt.g;
-                vP = vN;
-                pending = true;
-                if (mt.pos == mt.n - 1 && !resolve_pending()) return;
-            } else {
-                const int d = wait_dec(publish_block());
-                if (d < 0) return;
-                fold(tN, mbN, lbN);
-                if (d == kStop) {
-                    if (!epilogue(mt.b, mt.g)) return;
-                    reset();
-                    stopped_item = mt.item;
                 }
             }
-        } else {
-            fold(tN, mbN, lbN);
-            if (mt.pos == mt.n - 1) {
-                if (!epilogue(mt.b, mt.g)) return;
-                reset();
-                stopped_item = mt.item;
+            if (wg == 0 && lane == 0) {
+                SlotMeta& r = ctrl->info[rb];
+                r.kind = kind; r.item = mt.item; r.pos = mt.pos; r.n = mt.n; r.c = mt.c; r.has0 = mt.has0;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&part_full[rb]);
+        }
+    };
+
+    for (;;) {
+        const int slot = u % p.stages;
+        if (!wait_bounded(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
+        SlotMeta mt = meta[slot];
+        if (mt.kind < 0 || mt.kind > kSlotPad ||
+            (mt.kind == kSlotBlock && (mt.item < 0 || mt.item >= p.num_items || mt.nvalid < 1 || mt.nvalid > kBK ||
+                                       mt.pos < 0 || mt.pos >= mt.n || mt.b < 0 || mt.b >= p.B || mt.g < 0 ||
+                                       mt.g >= p.Hkv))) {
+            if (lane == 0) record_check(p.hdr, 5, u, mt.kind, mt.item);
+            mt.kind = kSlotPad;
+            mt.item = -2;
+        }
+        const bool is_data = mt.kind == kSlotBlock || mt.kind == kSlotPad;
+        const bool compute = mt.kind == kSlotBlock && mt.item != stopped_item;
+        if (compute) {
+            unsigned char* sK = ring + (size_t)slot * C::SLOT;
+            unsigned char* sV = sK + C::KVB;
+            if (mt.pos < NG) {
+                // the item's queries into this group's swizzled 8-row area (rows past G zero);
+                // the group's warps have finished the previous item's scores
+                const unsigned char* sQ = sK + 2 * C::KVB;
+                constexpr int QCH = 8 * (C::ROWB / 16);
+                for (int i = gtid; i < QCH; i += GW * 32) {
+                    const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                    const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
+                }
+                named_bar_sync(gbar, GW * 32);
+            }
+            const int nvalid = mt.nvalid;
+            // ---- S^T for this warp's 16 keys (two independent accumulation chains);
+            // ldmatrix / mma.sync / movmatrix are warp-aligned: reconverge before them
+            float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kbase = smem_addr(sK), vbase = smem_addr(sV);
+            __syncwarp();
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t b00, b01, b10, b11;
+                {
+                    const int c = 4 * kp + mi;
+                    ldsm_x4(qtbase + (uint32_t)((c >> 3) * 1024 + lr * 128 + (((c & 7) ^ lr) << 4)), b00, b01, b10, b11);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ks = 2 * kp + h;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(sw(kbase, keyK, 2 * ks + chK), a0, a1, a2, a3);
+                    mma_bf16(h ? s4b : s4, a0, a1, a2, a3, h ? b10 : b00, h ? b11 : b01);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s4[c] += s4b[c];
+            const int k0 = wg * 16 + grp, k1 = k0 + 8;
+            float sc[4];
+            sc[0] = (k0 < nvalid && v0) ? s4[0] * scale : -INFINITY;
+            sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
+            sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
+            sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
+            // ---- block max per head: over this warp's keys, then across the group
+            float m0 = fmaxf(sc[0], sc[2]), m1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            if (grp == 0) {
+                wmax[(bpar * NWC + w) * 8 + h0] = m0;
+                wmax[(bpar * NWC + w) * 8 + h1] = m1;
+            }
+            named_bar_sync(gbar, GW * 32);
+            float mb0 = -INFINITY, mb1 = -INFINITY;
+#pragma unroll
+            for (int ww = 0; ww < GW; ++ww) {
+                mb0 = fmaxf(mb0, wmax[(bpar * NWC + gi * GW + ww) * 8 + h0]);
+                mb1 = fmaxf(mb1, wmax[(bpar * NWC + gi * GW + ww) * 8 + h1]);
+            }
+            bpar ^= 1;
+            float pw[4];
+            pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mb0);
+            pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mb1);
+            pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - mb0);
+            pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - mb1);
+            float l0 = pw[0] + pw[2], l1 = pw[1] + pw[3];
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+            mbN[0] = mb0; mbN[1] = mb1; lbN[0] = l0; lbN[1] = l1;
+            // ---- P^T fragments: hi and lo bf16 parts, transposed by movmatrix
+            const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
+            const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
+            const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
+            __syncwarp();
+            const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB), bl0 = movm_t(lA), bl1 = movm_t(lB);
+            // ---- rows past the sequence end hold stale data: zero this warp's, so 0 * V stays 0
+            if (nvalid < wg * 16 + 16) {
+                const int r0 = max(nvalid, wg * 16);
+                const int nchunks = (wg * 16 + 16 - r0) * (C::ROWB / 16);
+                for (int i = lane; i < nchunks; i += 32) {
+                    const int row = r0 + i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                    *reinterpret_cast<uint4*>(sV + (c >> 3) * (kBK * 128) + row * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // ---- O^T partial of this block
+            __syncwarp();
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(sw(vbase, keyV, 2 * m + chV), a0, a1, a2, a3);
+                tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
+                mma_bf16(tN[m], a0, a1, a2, a3, bh0, bh1);
+                mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
             }
         }
-        advance();
+        __syncwarp();
+        if (lane == 0 && mt.kind != kSlotEnd) mbar_arrive(&empty[slot]);  // the slot's data are no longer read
+
+        // ---- this entry's record, then the decision on the previous one
+        publish(mt, (mt.kind == kSlotBlock && !compute) ? kSlotPad : mt.kind, compute);
+        bool ended = false;
+        if (pending) {
+            int d;
+            if (kART) {
+                d = wait_dec(uP);
+                if (d < 0) return;
+            } else {
+                d = !pcomp ? kDiscard : (posP == nP - 1 ? kStop : kContinue);
+            }
+            if (pcomp && d != kDiscard) fold(tP, mbP, lbP);
+            ended = (d == kStop || d == kDiscard) && itemP == cur_item;
+            pending = false;
+        }
+        if (cur_item != -1 && (ended || mt.item != cur_item || !is_data)) {
+            if (!finalize()) return;
+            reset();
+            stopped_item = cur_item;
+            cur_item = -1;
+        }
+        if (mt.kind == kSlotEnd) return;
+        if (!is_data && mt.pos == 0) write_zero(mt.b, mt.g);
+        if (is_data && cur_item == -1 && mt.item != stopped_item) {
+            cur_item = mt.item;
+            curb = mt.b;
+            curg = mt.g;
+        }
+        // this entry waits for its decision until this group's next entry
+        pending = true;
+        pcomp = compute;
+        uP = u;
+        itemP = mt.item;
+        posP = mt.pos;
+        nP = mt.n;
+        if (compute) {
+#pragma unroll
+            for (int m = 0; m < KS; ++m)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tP[m][c] = tN[m][c];
+            mbP[0] = mbN[0]; mbP[1] = mbN[1]; lbP[0] = lbN[0]; lbP[1] = lbN[1];
+        }
+        u += NG;
     }
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool kBF16, int D, int G>
+// one tensor-core group per CTA runs two CTAs per SM; two groups share one CTA per SM
+template <class C>
 struct MinBlocks {
-    static constexpr int value = Cfg<kBF16, D, G>::TC ? 2 : 1;
+    static constexpr int value = (C::TC && C::NG == 1) ? 2 : 1;
 };
 
-template <bool kBF16, int D, int G, bool kART>
-__global__ void __launch_bounds__(Cfg<kBF16, D, G>::THREADS, (MinBlocks<kBF16, D, G>::value))
+template <bool kBF16, int D, int G, int kNG, bool kART>
+__global__ void __launch_bounds__(Cfg<kBF16, D, G, kNG>::THREADS, (MinBlocks<Cfg<kBF16, D, G, kNG>>::value))
     art_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
-    using C = Cfg<kBF16, D, G>;
+    using C = Cfg<kBF16, D, G, kNG>;
     constexpr int NWC = C::NWC;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the swizzled tiles need a 1024-byte aligned ring
@@ -1288,8 +1333,8 @@ __global__ void __launch_bounds__(Cfg<kBF16, D, G>::THREADS, (MinBlocks<kBF16, D
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + p.stages;
     uint64_t* part_full = empty + p.stages;
-    uint64_t* dec_bar = part_full + 2;
-    uint64_t* cbar = dec_bar + 2;
+    uint64_t* dec_bar = part_full + C::NB;
+    uint64_t* cbar = dec_bar + C::NB;
     int* pmask = reinterpret_cast<int*>(smem + L.ptab);
     int* pbase = pmask + C::LPR;
     int* prank = pbase + C::LPR;
@@ -1299,16 +1344,16 @@ __global__ void __launch_bounds__(Cfg<kBF16, D, G>::THREADS, (MinBlocks<kBF16, D
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NWC);
+            mbar_init(&empty[s], C::GW);  // an entry is consumed by one group
         }
-        mbar_init(&part_full[0], NWC);
-        mbar_init(&part_full[1], NWC);
-        mbar_init(&dec_bar[0], 1);
-        mbar_init(&dec_bar[1], 1);
+        for (int b = 0; b < C::NB; ++b) {
+            mbar_init(&part_full[b], C::GW);
+            mbar_init(&dec_bar[b], 1);
+            ctrl->dec[b] = 0;
+        }
         mbar_init(cbar, NWC);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
-        ctrl->dec[0] = ctrl->dec[1] = 0;
         fence_mbar_init();
     }
     if (tid < C::LPR) {
@@ -1378,7 +1423,7 @@ inline EncodeTiledFn encode_tiled_fn() {
     if (!fn) {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(f);
     }
@@ -1400,21 +1445,14 @@ inline cudaError_t make_cache_map(CUtensorMap* m, const void* base, long long ro
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kBF16, int D, int G, bool kART>
-cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchInfo* li) {
-    using C = Cfg<kBF16, D, G>;
-    auto kern = art_decode_kernel<kBF16, D, G, kART>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    int sms = 0, smem_sm = 0, smem_blk = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
-        return e;
-    if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
-        return e;
+template <bool kBF16, int D, int G, int kNG, bool kART>
+cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, LaunchInfo* li, int sms, int smem_sm,
+                           int smem_blk) {
+    using C = Cfg<kBF16, D, G, kNG>;
+    auto kern = art_decode_kernel<kBF16, D, G, kNG, kART>;
+    cudaError_t e;
     // two CTAs per SM only pay when there are items for both
-    const int want = (MinBlocks<kBF16, D, G>::value > 1 && p.num_items > sms) ? 2 : 1;
+    const int want = (MinBlocks<C>::value > 1 && p.num_items > sms) ? 2 : 1;
     int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(want, smem_sm, smem_blk);
     if (stages == 0) stages = pick_stages<C>(1, smem_sm, smem_blk);
     if (stages == 0) return cudaErrorInvalidConfiguration;
@@ -1440,6 +1478,28 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
     if (li) { li->grid = grid; li->stages = stages; li->smem = smem; li->ctas_per_sm = occ; }
     kern<<<grid, C::THREADS, smem, stream>>>(p, tk, tv);
     return cudaGetLastError();
+}
+
+template <bool kBF16, int D, int G, bool kART>
+cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchInfo* li) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int sms = 0, smem_sm = 0, smem_blk = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    // bf16: with fewer items than two per SM, two consumer groups per CTA split each
+    // item's blocks; otherwise one group per CTA and two CTAs per SM
+    const char* env = std::getenv("ART_GROUPS");
+    const int groups = env ? std::atoi(env) : (p.num_items < 2 * sms ? 2 : 1);
+    if constexpr (kBF16) {
+        if (groups == 2)
+            return launch_variant<kBF16, D, G, 2, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+    }
+    return launch_variant<kBF16, D, G, 1, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
 }
 
 }  // namespace art
