@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--eps", type=float, default=None)
     ap.add_argument("--patience", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="replace the workload's batch (smaller profiler captures of the same kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -184,9 +186,11 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def load_traffic(config_name):
-    """DRAM bytes per launch of the decode kernel from a committed ncu summary,
-    only if it was taken on the current kernel source."""
+def load_traffic(config_name, alg_bytes):
+    """DRAM bytes (read + write) per decode-kernel launch from the committed ncu
+    summary of this workload, only if it was taken on the current kernel
+    source. A capture of a smaller batch of the same workload is scaled by the
+    algorithmic bytes of the two launches."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None, None
@@ -194,7 +198,10 @@ def load_traffic(config_name):
     e = d.get(config_name)
     if not e or e.get("kernel_hash") != kernel_source_hash():
         return None, None
-    return e.get("dram_bytes_per_launch"), e
+    t = float(e["dram_bytes"]) * alg_bytes / float(e["algorithmic_bytes"])
+    src = f"ncu capture of {e['captured_workload']}" + \
+        ("" if e["captured_workload"] == config_name else ", scaled by algorithmic bytes")
+    return t, src
 
 
 def cpu_baseline(w, eps, p, budget_s=12.0):
@@ -217,6 +224,13 @@ def cpu_baseline(w, eps, p, budget_s=12.0):
             "seconds_per_run": t}
 
 
+def config_dict(w, eps, p, ws):
+    return {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "page_size": w.page_size, "block_size": w.block_size, "eps": eps,
+            "patience": p, "l2": "flushed (256 MB write) before every timed call; inputs also exceed L2",
+            "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"}
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle timed as it stands on the host cores
 # ---------------------------------------------------------------------------
@@ -224,7 +238,7 @@ def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    w = W.config(args.config, eps=args.eps, patience=args.patience)
+    w = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)
     eps, p = w.eps_mag, w.patience
     import oracle as O
     # each step: the oracle over a bounded sample of items (at most ~10 s per step)
@@ -249,7 +263,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "items_per_step": int(k), "eps": eps, "patience": p},
+            "config": dict(config_dict(w, eps, p, ws=1), items_per_step=int(k)),
             "cpu_baseline": {"value": value, "unit": "queries/s", "cores": int(nt), "kind": "oracle",
                              "sample": f"{k} of {n_items} (sequence, KV head) items per step"},
             "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -271,7 +285,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     B.build()
-    w = W.config(args.config, eps=args.eps, patience=args.patience)  # one full replica per rank
+    w = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)  # one replica per rank
     eps, p = w.eps_mag, w.patience
     dev = K.DeviceInputs(w)
     queries = w.batch * w.num_q_heads
@@ -284,16 +298,33 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def time_calls(fn, steps):
+    def events(steps):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:  # record once so that the CUDA events exist
+            a.record(stream)
+            b.record(stream)
+        return evs
+
+    def time_calls(fn, steps, kernel=False):
+        """Per-call times (ms) with CUDA events on the launching stream; with
+        `kernel`, also the decode kernel alone (events recorded by libart right
+        around its launch)."""
+        evs, kev = events(steps), events(steps) if kernel else None
         barrier()
         for i in range(steps):
             flush.fill_(i & 255)
             evs[i][0].record(stream)
+            if kernel:
+                K.set_timing_events(*kev[i])
             fn()
             evs[i][1].record(stream)
+        if kernel:
+            K.set_timing_events()
         barrier()
-        return np.array([a.elapsed_time(b) for a, b in evs])  # ms
+        t = np.array([a.elapsed_time(b) for a, b in evs])
+        if not kernel:
+            return t
+        return t, np.array([a.elapsed_time(b) for a, b in kev])
 
     art_call = lambda: dev.art(eps, eps, p, stream=stream)
     dense_call = lambda: dev.dense(stream=stream)
@@ -307,9 +338,10 @@ def run_ours(args):
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
     time.sleep(0.3)
-    t_art = time_calls(art_call, args.steps)
+    t_art, t_kern = time_calls(art_call, args.steps, kernel=True)
     clocks = clk.stop()
     ms = max_over_ranks(float(t_art.mean()), device="cuda")
+    ms_kernel = max_over_ranks(float(t_kern.mean()), device="cuda")
     value = ws * queries / (ms * 1e-3)
 
     # dense twin on the same buffers
@@ -317,10 +349,11 @@ def run_ours(args):
     if not args.no_dense:
         for _ in range(max(3, args.warmup)):
             dense_call()
-        t_d = time_calls(dense_call, args.steps)
-        ms_d = float(t_d.mean())
-        dense = {"queries_per_s": queries / (ms_d * 1e-3), "ms_per_step": ms_d,
-                 "gbs": (kv_bytes(w) + side_bytes(w)) / (ms_d * 1e-3) / 1e9, "speedup_art_over_dense": ms_d / ms}
+        t_d, t_dk = time_calls(dense_call, args.steps, kernel=True)
+        ms_d, ms_dk = float(t_d.mean()), float(t_dk.mean())
+        dense = {"queries_per_s": queries / (ms_d * 1e-3), "ms_per_step": ms_d, "kernel_ms": ms_dk,
+                 "kernel_gbs": (kv_bytes(w) + side_bytes(w)) / (ms_dk * 1e-3) / 1e9,
+                 "speedup_art_over_dense": ms_d / ms}
         # the detector's own cost: ART with eps = 0 never stops
         zero = lambda: dev.art(0.0, 0.0, p, stream=stream)
         for _ in range(3):
@@ -332,11 +365,15 @@ def run_ours(args):
     # roofline of the decode kernel (bytes actually needed by the blocks processed)
     peak, peak_kind = load_peaks()
     alg = kv_bytes(w, bu) + side_bytes(w)
-    achieved = alg / (ms * 1e-3) / 1e9
-    traffic, _ = load_traffic(w.name)
+    achieved = alg / (ms_kernel * 1e-3) / 1e9
+    traffic, traffic_src = load_traffic(w.name, alg)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg,
-                "timed": "whole art_decode call (workspace memset + plan kernel + decode kernel)"}
+                "traffic": traffic, "traffic_source": traffic_src, "peak_kind": peak_kind,
+                "kernel": "art_decode_kernel", "algorithmic_bytes_per_launch": alg,
+                "kernel_ms_per_launch": ms_kernel,
+                "kernel_ms_median_min_max": [float(np.median(t_kern)), float(t_kern.min()), float(t_kern.max())],
+                "timed": "decode kernel alone, CUDA events recorded by libart around its launch",
+                "call_achieved_gbs": alg / (ms * 1e-3) / 1e9}
 
     # end to end through the public API with host buffers: per step the step's
     # inputs (queries, lengths, page table, visit lists) go host->device and the
@@ -379,11 +416,7 @@ def run_ours(args):
                 "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-                "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
-                           "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
-                           "block_size": w.block_size, "eps": eps, "patience": p,
-                           "l2": "flushed (256 MB write) before every timed call; inputs also exceed L2",
-                           "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
+                "config": config_dict(w, eps, p, ws),
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": 2 * args.steps,
                 "dense_twin": dense,

@@ -183,6 +183,17 @@ const char* art_status_string(int code);
 /* Text of the last CUDA error seen by this library in the calling thread. */
 const char* art_last_cuda_error(void);
 
+/*
+ * Measurement hook (an addition of this library; the ART paper has none).
+ * `start` and `stop` are cudaEvent_t handles passed as void*, owned by the
+ * caller. While set, every art_decode / dense_decode / art_decode_static call
+ * made by the calling thread records `start` on its stream right before the
+ * decode-kernel launch and `stop` right after it, so that cudaEventElapsedTime
+ * gives the decode kernel alone (without the workspace memset and the plan
+ * kernel). A call that fails its checks records neither. NULL, NULL clears.
+ */
+void art_set_timing_events(void* start, void* stop);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,8 +21,8 @@ ART_DTYPE_BF16, ART_DTYPE_F32 = 0, 1
 ART_OK, ART_ERR_INVALID_ARG, ART_ERR_UNSUPPORTED, ART_ERR_WORKSPACE, ART_ERR_LAUNCH = 0, -1, -2, -3, -4
 STATUS_BITS = {1: "bad visit entry", 2: "duplicate visit entry", 4: "bad page id", 8: "bad seq_len",
                16: "bad probe index", 32: "wait timeout", 64: "internal check failed"}
-EXPORTS = ("art_workspace_bytes", "art_decode", "dense_decode", "art_read_device_status",
-           "art_status_string", "art_last_cuda_error")
+EXPORTS = ("art_workspace_bytes", "art_decode", "dense_decode", "art_decode_static", "art_read_device_status",
+           "art_status_string", "art_last_cuda_error", "art_set_timing_events")
 
 
 class ArtShape(ctypes.Structure):
@@ -62,6 +62,10 @@ def lib(path: str = LIB_PATH) -> ctypes.CDLL:
             L.art_status_string.restype = ctypes.c_char_p
             L.art_last_cuda_error.argtypes = []
             L.art_last_cuda_error.restype = ctypes.c_char_p
+            L.art_decode_static.argtypes = [P, P, P, P, P, P, F32, F32, I32, P, P, P, SP, P]
+            L.art_decode_static.restype = ctypes.c_int
+            L.art_set_timing_events.argtypes = [P, P]
+            L.art_set_timing_events.restype = None
             _lib = L
     return _lib
 
@@ -126,6 +130,26 @@ def dense_decode(q, k_cache, v_cache, block_table, seq_lens, visit_order, out, s
     if check:
         _check(rc)
     return rc
+
+
+def art_decode_static(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience,
+                      probe_idx, out, blocks_used, shape: ArtShape, stream=None, check: bool = True) -> int:
+    """art_decode with the library's own fixed device scratch instead of a workspace."""
+    rc = lib().art_decode_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+                                 _ptr(visit_order), float(eps_mag), float(eps_dir), int(patience),
+                                 _ptr(probe_idx), _ptr(out), _ptr(blocks_used), ctypes.byref(shape),
+                                 _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def set_timing_events(start=None, stop=None):
+    """Have this thread's next calls record `start` / `stop` (torch.cuda.Event,
+    already recorded once so that they exist) around the decode-kernel launch;
+    no arguments clears."""
+    h = lambda e: None if e is None else ctypes.c_void_p(int(e.cuda_event))
+    lib().art_set_timing_events(h(start), h(stop))
 
 
 def art_read_device_status(workspace) -> int:

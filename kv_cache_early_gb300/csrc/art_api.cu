@@ -187,6 +187,12 @@ static cudaError_t dispatch(const art_shape& s, const Params& p, cudaStream_t st
     return cudaErrorInvalidValue;
 }
 
+// events recorded around the decode-kernel launch of this thread's calls
+struct TimingEvents {
+    cudaEvent_t start = nullptr, stop = nullptr;
+};
+static thread_local TimingEvents t_events;
+
 static int env_stages() {
     const char* e = std::getenv("ART_STAGES");
     return e ? std::atoi(e) : 0;
@@ -264,8 +270,10 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     p.eps_mag = eps_mag;
     p.eps_dir = eps_dir;
     p.patience = patience;
+    if (t_events.start && (e = cudaEventRecord(t_events.start, st)) != cudaSuccess) return cuda_fail(e);
     e = dispatch<kART>(s, p, st, env_stages(), li);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (t_events.stop && (e = cudaEventRecord(t_events.stop, st)) != cudaSuccess) return cuda_fail(e);
     return ART_OK;
 }
 
@@ -315,6 +323,11 @@ const char* art_status_string(int code) {
 }
 
 const char* art_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+void art_set_timing_events(void* start, void* stop) {
+    t_events.start = static_cast<cudaEvent_t>(start);
+    t_events.stop = static_cast<cudaEvent_t>(stop);
+}
 
 }  // extern "C"
 

@@ -101,6 +101,42 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// one arrive from the lanes where `pred` holds (typically one lane), without a branch
+__device__ __forceinline__ void mbar_arrive_if(bool pred, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q mbarrier.arrive.shared::cta.b64 _, [%1];\n\t}" ::"r"((int)pred),
+        "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Predicated shared-memory stores: lanes store or not without a divergent branch.
+__device__ __forceinline__ void st_shared_if(bool pred, int* p, int v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q st.shared.b32 [%1], %2;\n\t}" ::"r"((int)pred),
+        "r"(smem_addr(p)), "r"(v)
+        : "memory");
+}
+__device__ __forceinline__ void st_shared_if(bool pred, float* p, float v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q st.shared.f32 [%1], %2;\n\t}" ::"r"((int)pred),
+        "r"(smem_addr(p)), "f"(v)
+        : "memory");
+}
+__device__ __forceinline__ void st_shared_if(bool pred, float* p, float x, float y) {  // p 8-byte aligned
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q st.shared.v2.f32 [%1], {%2, %3};\n\t}" ::"r"((int)pred),
+        "r"(smem_addr(p)), "f"(x), "f"(y)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");

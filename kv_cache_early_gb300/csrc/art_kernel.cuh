@@ -84,9 +84,18 @@ struct Cfg {
     static constexpr int QB = (int)align_up((size_t)G * D * ELT, 16);
     static constexpr int KVB = kBK * ROWB;       // bytes of K (or V) of one block
     static constexpr int SLOT = (int)align_up((size_t)2 * KVB + QB, TC ? 1024 : 16);
-    static constexpr int SPL = (G * kMaxProbe + 31) / 32;  // probe slots per stat lane
-    static constexpr int PRW = TC ? 1 : RPW;     // probe partial rows per warp
-    static constexpr int PART_F = NB * GW * PRW * G * kMaxProbe;
+    // probe partial rows: word s * GP + h holds probe rank s of head h (GP even, so a
+    // lane's pair of adjacent heads is one 8-byte store); rows padded by 8 words so
+    // that the high- and low-part rows of the split tile fall in other banks
+    static constexpr int GP = (G + 1) & ~1;
+    static constexpr int PST = kMaxProbe * GP + 8;
+    static constexpr int SPL = (kMaxProbe * GP + 31) / 32;  // probe slots per stat lane
+    static_assert(32 % GP == 0, "a stat lane's slots share one head");
+    // G <= 4: the P.V products put the bf16 high parts of P in columns 0-3 of the
+    // 8-wide tile and the low parts in columns 4-7, one mma per m-tile
+    static constexpr bool SPLITN = TC && G <= 4;
+    static constexpr int PRW = TC ? (SPLITN ? 2 : 1) : RPW;  // probe partial rows per warp
+    static constexpr int PART_F = NB * GW * PRW * PST;
     static constexpr int KS = D / 16;            // tensor-core k-steps (QK) and m-tiles (PV)
     static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
     static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
@@ -122,12 +131,12 @@ __host__ __device__ inline Layout make_layout(int stages) {
     L.bars = o;
     o += (size_t)(2 * stages + 2 * C::NB + 1) * sizeof(uint64_t);
     o = align_up(o, 16);
-    L.part = o;  // [2][NWC][RPW][G][kMaxProbe] probe partials
+    L.part = o;  // [NB][GW][PRW][PST] probe partial rows
     o += (size_t)C::PART_F * sizeof(float);
     L.plb = o;  // [NB][GW][G] per-warp block sums
     o += (size_t)C::NB * C::GW * G * sizeof(float);
-    L.pmb = o;  // [NB][G] block maxima
-    o += (size_t)C::NB * G * sizeof(float);
+    L.pmb = o;  // [NB][GW][G] per-warp block maxima
+    o += (size_t)C::NB * C::GW * G * sizeof(float);
     L.wmax = o;  // [2][NWC][8] per-warp maxima of the block being processed (by block parity)
     o += (size_t)2 * C::NWC * 8 * sizeof(float);
     L.scr = o;  // [NWC][G][RW] scores, then weights
@@ -416,28 +425,30 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
                           uint64_t* part_full, uint64_t* dec_bar, Ctrl* ctrl) {
     constexpr int G = C::GQ;
     constexpr int SPL = C::SPL;
-    constexpr int NP = C::GW * C::PRW;  // partial rows per probe slot
+    constexpr int NP = C::GW * C::PRW;  // partial rows per record
     constexpr int NB = C::NB;
     (void)sh;
     const int lane = threadIdx.x & 31;
     const int m = p.m;
-    const int GM = G * m;
-    // the probe slot of each (lane, j): head, and its offset in a partial row
-    int hs[SPL], off[SPL];
+    // probe slot k = lane + 32 j is word k of a partial row: head k % GP, rank k / GP
+    // (the statistics do not depend on the order of the probe coordinates)
+    int hs[SPL];
 #pragma unroll
     for (int j = 0; j < SPL; ++j) {
         const int k = lane + 32 * j;
-        hs[j] = k < GM ? k / m : -1;
-        off[j] = k < GM ? (k / m) * kMaxProbe + (k - (k / m) * m) : 0;
+        hs[j] = (k % C::GP < G && k / C::GP < m) ? k % C::GP : -1;
     }
-    float M[G], Lsum[G];  // running max / sum per head (every lane keeps all heads)
+    // every slot of this lane belongs to head lane % GP, whose running max and
+    // weight sum the lane keeps
+    const int hme = lane % C::GP < G ? lane % C::GP : 0;
+    float M = -INFINITY, Lsum = 0.f;
     float X[SPL];
     float nprev = 0.f;  // |x_{i-1}|
     int counter = 0, seen0 = 0;
     int stopped_item = -1;
     auto reset = [&]() {
-#pragma unroll
-        for (int h = 0; h < G; ++h) { M[h] = -INFINITY; Lsum[h] = 0.f; }
+        M = -INFINITY;
+        Lsum = 0.f;
 #pragma unroll
         for (int j = 0; j < SPL; ++j) X[j] = 0.f;
         nprev = 0.f;
@@ -446,10 +457,8 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
     };
     auto send = [&](int vb, int dec) {
         __syncwarp();
-        if (lane == 0) {
-            ctrl->dec[vb] = dec;
-            mbar_arrive(&dec_bar[vb]);
-        }
+        st_shared_if(lane == 0, &ctrl->dec[vb], dec);
+        mbar_arrive_if(lane == 0, &dec_bar[vb]);
     };
     reset();
     for (int v = 0;; ++v) {
@@ -484,43 +493,47 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
             send(vb, last ? kStop : kContinue);
             sent = true;
         }
-        // per head: block sum over the warps, new running max and sum, and the
-        // factor that moves the probe: delta = coef_h * (PV_probe - l_blk,h * x)
-        float coef[G], lbh[G];
-        const float* pp = part + (size_t)vb * NP * G * kMaxProbe;
+        // block max and sum of this lane's head over the consumer warps (each warp
+        // used its own max), new running max and sum, and the factor that moves
+        // the probe: delta = cf * (PV_probe - l_blk * x)
+        float sw[C::GW];
+        float mbk = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float mb = pmb[vb * G + h];
-            float lb = 0.f;
-#pragma unroll
-            for (int w = 0; w < C::GW; ++w) lb += plb[(vb * C::GW + w) * G + h];
-            const float Mn = fmaxf(M[h], mb);
-            const float a = exp2f(M[h] - Mn);
-            const float bw = exp2f(mb - Mn);
-            const float Ln = a * Lsum[h] + bw * lb;
-            coef[h] = bw / Ln;
-            lbh[h] = lb;
-            M[h] = Mn;
-            Lsum[h] = Ln;
+        for (int w = 0; w < C::GW; ++w) {
+            sw[w] = pmb[(vb * C::GW + w) * G + hme];
+            mbk = fmaxf(mbk, sw[w]);
         }
+        float lb = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::GW; ++w) {
+            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a warp without valid keys adds nothing
+            lb = fmaf(sw[w], plb[(vb * C::GW + w) * G + hme], lb);
+        }
+        const float Mn = fmaxf(M, mbk);
+        const float a = exp2f(M - Mn);
+        const float bw = exp2f(mbk - Mn);
+        const float Ln = fmaf(a, Lsum, bw * lb);
+        const float cf = __fdividef(bw, Ln);  // Ln >= 1: the block's largest weight is 1 after rescaling
+        M = Mn;
+        Lsum = Ln;
+        const float* pp = part + (size_t)vb * NP * C::PST;
         float s1 = 0.f, s2 = 0.f, s3 = 0.f;  // sum delta^2, sum delta . x_{i-1}, |x_i|^2
 #pragma unroll
         for (int j = 0; j < SPL; ++j) {
-            const int h = hs[j];
-            if (h >= 0) {
-                float pb = 0.f;
+            float pb = 0.f;
 #pragma unroll
-                for (int w = 0; w < NP; ++w) pb += pp[w * G * kMaxProbe + off[j]];
-                float cf = 0.f, lb = 0.f;
+            for (int w = 0; w < C::GW; ++w) {
+                float pw = 0.f;
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    if (hh == h) { cf = coef[hh]; lb = lbh[hh]; }
-                const float d = cf * (pb - lb * X[j]);
-                s1 = fmaf(d, d, s1);
-                s2 = fmaf(d, X[j], s2);
-                X[j] += d;
-                s3 = fmaf(X[j], X[j], s3);
+                for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
+                pb = fmaf(sw[w], pw, pb);
             }
+            // slots past the probe (or past G) hold no data: no change
+            const float d = hs[j] >= 0 ? cf * (pb - lb * X[j]) : 0.f;
+            s1 = fmaf(d, d, s1);
+            s2 = fmaf(d, X[j], s2);
+            X[j] += d;
+            s3 = fmaf(X[j], X[j], s3);
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
@@ -530,17 +543,16 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         }
         // |x_i| - |x_{i-1}| = (|x_i|^2 - |x_{i-1}|^2) / (|x_i| + |x_{i-1}|) with the
         // difference of squares formed directly as 2 s2 + s1;
-        // 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2 = (s1 - 2 s2 dn / n_{i-1} + dn^2) / (2 |x_i|^2)
+        // 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2 = (s1 - 2 s2 dn / n_{i-1} + dn^2) / (2 |x_i|^2).
+        // Fast divisions (a few ulp): the results only meet the thresholds, whose
+        // decisions are exact up to a tie zone far wider than that.
         const float ni = sqrtf(s3);
-        bool stable = false;
-        if (pos >= 1) {
-            const float dn = (2.f * s2 + s1) / (ni + nprev);
-            const float rprev = 1.f / nprev;
-            const float dmag = fabsf(dn) * rprev;
-            const float ddir = fmaxf(0.f, (s1 - 2.f * s2 * (dn * rprev) + dn * dn) / (2.f * s3));
-            stable = nprev > 0.f && ni > 0.f && isfinite(nprev) && isfinite(ni) && isfinite(dmag) &&
-                     isfinite(ddir) && dmag < p.eps_mag && ddir < p.eps_dir;
-        }
+        const float dn = __fdividef(2.f * s2 + s1, ni + nprev);
+        const float rprev = __fdividef(1.f, nprev);
+        const float dmag = fabsf(dn) * rprev;
+        const float ddir = fmaxf(0.f, __fdividef(s1 - 2.f * s2 * (dn * rprev) + dn * dn, 2.f * s3));
+        const bool stable = pos >= 1 && nprev > 0.f && ni > 0.f && nprev < 1e30f && ni < 1e30f &&
+                            dmag < p.eps_mag && ddir < p.eps_dir;
         nprev = ni;
         counter = stable ? counter + 1 : 0;
         const bool stop = last || (may_stop && counter >= p.patience);
@@ -625,7 +637,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     };
     auto release = [&]() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        mbar_arrive_if(lane == 0, &empty[slot]);
     };
     auto advance = [&]() {
         if (++slot == p.stages) { slot = 0; ++round; }
@@ -637,7 +649,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
         const int vb = v & 1;
         if (w == 0 && lane == 0) ctrl->info[vb] = mt;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&part_full[vb]);
+        mbar_arrive_if(lane == 0, &part_full[vb]);
         return v++;
     };
     auto wait_dec = [&](int rec) -> int {
@@ -860,7 +872,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
         if (kART) {
             // probe partials of this lane's rows: slot rank = probe columns before it
             const int vb = v & 1;
-            float* pp = part + (((size_t)vb * kNWC + w) * RPW + half) * G * kMaxProbe;
+            float* pp = part + (((size_t)vb * kNWC + w) * RPW + half) * C::PST;
 #pragma unroll
             for (int e = 0; e < EPC; ++e) {
                 if ((my_mask >> e) & 1u) {
@@ -869,7 +881,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
                     for (int h = 0; h < G; ++h) {
                         float lo, hi;
                         up2(tN[h][e >> 1], lo, hi);
-                        pp[h * kMaxProbe + s] = (e & 1) ? hi : lo;
+                        pp[s * C::GP + h] = (e & 1) ? hi : lo;
                     }
                 }
             }
@@ -877,9 +889,9 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
 #pragma unroll
                 for (int h = 0; h < G; ++h) plb[(vb * kNWC + w) * G + h] = lbN[h];
             }
-            if (w == 0 && lane == 0) {
+            if (lane == 0) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) pmb[vb * G + h] = mbN[h];
+                for (int h = 0; h < G; ++h) pmb[(vb * kNWC + w) * G + h] = mbN[h];
             }
             const int vN = publish(mt);
             if (LAG) {
@@ -965,11 +977,17 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
     const int gi = w / GW, wg = w % GW;  // group, warp within the group
     const int grp = lane >> 2, tig = lane & 3;
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
-    const bool v0 = h0 < G, v1 = h1 < G;
+    const bool v0 = h0 < G, v1 = h1 < G;  // the score columns of this lane hold real heads
+    // the O^T columns of this lane: heads (q0, q1); with the split tile, lanes with
+    // tig >= 2 hold the low parts of heads 2 tig - 4, 2 tig - 3
+    constexpr bool SPLITN = C::SPLITN;
+    const bool lo_lane = SPLITN && tig >= 2;
+    const int q0 = lo_lane ? h0 - 4 : h0, q1 = q0 + 1;
+    const bool u0 = q0 < G, u1 = q1 < G;          // columns that belong to a real head
+    const bool w0 = u0 && !lo_lane, w1 = u1 && !lo_lane;  // ... and are written by this lane
     float* part = reinterpret_cast<float*>(smem + L.part);
     float* plb = reinterpret_cast<float*>(smem + L.plb);
     float* pmb = reinterpret_cast<float*>(smem + L.pmb);
-    float* wmax = reinterpret_cast<float*>(smem + L.wmax);
     float* eacc = reinterpret_cast<float*>(smem + L.eacc);
     unsigned char* sQt = smem + L.qt + (size_t)gi * 8 * C::ROWB;
     const uint32_t qtbase = smem_addr(sQt);
@@ -1022,7 +1040,6 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
     mbN[0] = mbN[1] = mbP[0] = mbP[1] = lbN[0] = lbN[1] = lbP[0] = lbP[1] = 0.f;
 
     int u = gi;            // this group's current ring entry (= its record number)
-    int bpar = 0;          // parity of the blocks this group computed (wmax buffer)
     uint32_t cbph = 0;     // phase of the all-consumer barrier
     int cur_item = -1, curb = 0, curg = 0;  // the item held in this group's accumulators
     int stopped_item = -1;                  // the last item this group ended
@@ -1047,15 +1064,11 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
         float a[2], bb[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            if (mb[j] == -INFINITY) {  // a head beyond G, or no valid key
-                a[j] = 1.f;
-                bb[j] = 0.f;
-                continue;
-            }
-            const float mn = fmaxf(mrun[j], mb[j]);
-            a[j] = exp2f(mrun[j] - mn);
-            bb[j] = exp2f(mb[j] - mn);
-            lrun[j] = a[j] * lrun[j] + bb[j] * lb[j];
+            const bool none = mb[j] == -INFINITY;  // a head beyond G, or no valid key: keep the state
+            const float mn = none ? mrun[j] : fmaxf(mrun[j], mb[j]);
+            a[j] = none ? 1.f : exp2f(mrun[j] - mn);
+            bb[j] = none ? 0.f : exp2f(mb[j] - mn);
+            lrun[j] = none ? lrun[j] : a[j] * lrun[j] + bb[j] * lb[j];
             mrun[j] = mn;
         }
 #pragma unroll
@@ -1067,17 +1080,24 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
     // has its own running maxima) and write O = sum / weight sum
     auto finalize = [&]() -> bool {
         float* mine = eacc + (size_t)w * (G * D + 2 * G);
+        if constexpr (SPLITN) {
+            // high + low parts (both lanes carry the same running max and sum)
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[mt][c] += __shfl_xor_sync(0xffffffffu, acc[mt][c], 2);
+        }
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int d = 16 * mt + grp + 8 * r;
-                if (v0) mine[h0 * D + d] = acc[mt][2 * r];
-                if (v1) mine[h1 * D + d] = acc[mt][2 * r + 1];
+                if (w0) mine[q0 * D + d] = acc[mt][2 * r];
+                if (w1) mine[q1 * D + d] = acc[mt][2 * r + 1];
             }
         if (grp == 0) {
-            if (v0) { mine[G * D + h0] = lrun[0]; mine[G * D + G + h0] = mrun[0]; }
-            if (v1) { mine[G * D + h1] = lrun[1]; mine[G * D + G + h1] = mrun[1]; }
+            if (w0) { mine[G * D + q0] = lrun[0]; mine[G * D + G + q0] = mrun[0]; }
+            if (w1) { mine[G * D + q1] = lrun[1]; mine[G * D + G + q1] = mrun[1]; }
         }
         if (!cbar_sync()) return false;
         const int ob = curb, og = curg;  // both groups hold the same item
@@ -1113,31 +1133,30 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
         const int rb = u % NB;
         if (kART) {
             if (computed) {
-                float* pp = part + ((size_t)rb * GW + wg) * G * kMaxProbe;
+                // probe partial rows: one per warp, two (high, low) with the split tile;
+                // predicated stores, no divergent branches
+                float* pp = part + (((size_t)rb * GW + wg) * C::PRW + (lo_lane ? 1 : 0)) * C::PST + q0;
 #pragma unroll
                 for (int m = 0; m < KS; ++m)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const bool on = (pbits >> (2 * m + r)) & 1u;
                         const int rank = (int)((prk[(2 * m + r) >> 2] >> (8 * ((2 * m + r) & 3))) & 0xffu);
-                        if (on && v0) pp[h0 * kMaxProbe + rank] = tN[m][2 * r];
-                        if (on && v1) pp[h1 * kMaxProbe + rank] = tN[m][2 * r + 1];
+                        float* dst = pp + rank * C::GP;
+                        if (G >= 2) st_shared_if(on && u1, dst, tN[m][2 * r], tN[m][2 * r + 1]);
+                        if (G % 2) st_shared_if(on && u0 && !u1, dst, tN[m][2 * r]);
                     }
-                if (grp == 0) {
-                    if (v0) plb[(rb * GW + wg) * G + h0] = lbN[0];
-                    if (v1) plb[(rb * GW + wg) * G + h1] = lbN[1];
-                    if (wg == 0) {
-                        if (v0) pmb[rb * G + h0] = mbN[0];
-                        if (v1) pmb[rb * G + h1] = mbN[1];
-                    }
-                }
+                st_shared_if(grp == 0 && w0, &plb[(rb * GW + wg) * G + (w0 ? q0 : 0)], lbN[0]);
+                st_shared_if(grp == 0 && w1, &plb[(rb * GW + wg) * G + (w1 ? q1 : 0)], lbN[1]);
+                st_shared_if(grp == 0 && w0, &pmb[(rb * GW + wg) * G + (w0 ? q0 : 0)], mbN[0]);
+                st_shared_if(grp == 0 && w1, &pmb[(rb * GW + wg) * G + (w1 ? q1 : 0)], mbN[1]);
             }
             if (wg == 0 && lane == 0) {
                 SlotMeta& r = ctrl->info[rb];
                 r.kind = kind; r.item = mt.item; r.pos = mt.pos; r.n = mt.n; r.c = mt.c; r.has0 = mt.has0;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&part_full[rb]);
+            mbar_arrive_if(lane == 0, &part_full[rb]);
         }
     };
 
@@ -1159,8 +1178,9 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
             unsigned char* sK = ring + (size_t)slot * C::SLOT;
             unsigned char* sV = sK + C::KVB;
             if (mt.pos < NG) {
-                // the item's queries into this group's swizzled 8-row area (rows past G zero);
-                // the group's warps have finished the previous item's scores
+                // the item's queries into this group's swizzled 8-row area (rows past G zero),
+                // once every warp of the group has finished the previous item's scores
+                named_bar_sync(gbar, GW * 32);
                 const unsigned char* sQ = sK + 2 * C::KVB;
                 constexpr int QCH = 8 * (C::ROWB / 16);
                 for (int i = gtid; i < QCH; i += GW * 32) {
@@ -1200,25 +1220,14 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
             sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
             sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
             sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
-            // ---- block max per head: over this warp's keys, then across the group
-            float m0 = fmaxf(sc[0], sc[2]), m1 = fmaxf(sc[1], sc[3]);
+            // ---- this warp's block max per head (each warp keeps its own running max;
+            // the statistics warp and the item's final merge rescale between warps)
+            float mb0 = fmaxf(sc[0], sc[2]), mb1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
-                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                mb0 = fmaxf(mb0, __shfl_xor_sync(0xffffffffu, mb0, o));
+                mb1 = fmaxf(mb1, __shfl_xor_sync(0xffffffffu, mb1, o));
             }
-            if (grp == 0) {
-                wmax[(bpar * NWC + w) * 8 + h0] = m0;
-                wmax[(bpar * NWC + w) * 8 + h1] = m1;
-            }
-            named_bar_sync(gbar, GW * 32);
-            float mb0 = -INFINITY, mb1 = -INFINITY;
-#pragma unroll
-            for (int ww = 0; ww < GW; ++ww) {
-                mb0 = fmaxf(mb0, wmax[(bpar * NWC + gi * GW + ww) * 8 + h0]);
-                mb1 = fmaxf(mb1, wmax[(bpar * NWC + gi * GW + ww) * 8 + h1]);
-            }
-            bpar ^= 1;
             float pw[4];
             pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mb0);
             pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mb1);
@@ -1230,13 +1239,34 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
                 l0 += __shfl_xor_sync(0xffffffffu, l0, o);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, o);
             }
-            mbN[0] = mb0; mbN[1] = mb1; lbN[0] = l0; lbN[1] = l1;
-            // ---- P^T fragments: hi and lo bf16 parts, transposed by movmatrix
-            const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
-            const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
-            const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
-            __syncwarp();
-            const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB), bl0 = movm_t(lA), bl1 = movm_t(lB);
+            uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+            if constexpr (SPLITN) {
+                // low-part lanes take the weights, maxima and sums of lane ^ 2
+                float px[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) px[c] = __shfl_xor_sync(0xffffffffu, pw[c], 2);
+                const float mx0 = __shfl_xor_sync(0xffffffffu, mb0, 2), mx1 = __shfl_xor_sync(0xffffffffu, mb1, 2);
+                const float lx0 = __shfl_xor_sync(0xffffffffu, l0, 2), lx1 = __shfl_xor_sync(0xffffffffu, l1, 2);
+                float t[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) t[c] = lo_lane ? px[c] : pw[c];
+                mbN[0] = lo_lane ? mx0 : mb0; mbN[1] = lo_lane ? mx1 : mb1;
+                lbN[0] = lo_lane ? lx0 : l0; lbN[1] = lo_lane ? lx1 : l1;
+                const uint32_t hA = pack_bf16(t[0], t[1]), hB = pack_bf16(t[2], t[3]);
+                const uint32_t lA = pack_bf16(t[0] - bf16_lo_f(hA), t[1] - bf16_hi_f(hA));
+                const uint32_t lB = pack_bf16(t[2] - bf16_lo_f(hB), t[3] - bf16_hi_f(hB));
+                __syncwarp();
+                bh0 = movm_t(lo_lane ? lA : hA);
+                bh1 = movm_t(lo_lane ? lB : hB);
+            } else {
+                mbN[0] = mb0; mbN[1] = mb1; lbN[0] = l0; lbN[1] = l1;
+                // ---- P^T fragments: hi and lo bf16 parts, transposed by movmatrix
+                const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
+                const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
+                const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
+                __syncwarp();
+                bh0 = movm_t(hA); bh1 = movm_t(hB); bl0 = movm_t(lA); bl1 = movm_t(lB);
+            }
             // ---- rows past the sequence end hold stale data: zero this warp's, so 0 * V stays 0
             if (nvalid < wg * 16 + 16) {
                 const int r0 = max(nvalid, wg * 16);
@@ -1257,11 +1287,11 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
                 ldsm_x4_t(sw(vbase, keyV, 2 * m + chV), a0, a1, a2, a3);
                 tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
                 mma_bf16(tN[m], a0, a1, a2, a3, bh0, bh1);
-                mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
+                if constexpr (!SPLITN) mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
             }
         }
         __syncwarp();
-        if (lane == 0 && mt.kind != kSlotEnd) mbar_arrive(&empty[slot]);  // the slot's data are no longer read
+        mbar_arrive_if(lane == 0 && mt.kind != kSlotEnd, &empty[slot]);  // the slot's data are no longer read
 
         // ---- this entry's record, then the decision on the previous one
         publish(mt, (mt.kind == kSlotBlock && !compute) ? kSlotPad : mt.kind, compute);

@@ -320,24 +320,34 @@ CONFIG_NAMES = {
 
 
 def config(k: int, *, small: bool = False, eps: Optional[float] = None, patience: Optional[int] = None,
-           threads: Optional[int] = None) -> Workload:
+           threads: Optional[int] = None, batch: Optional[int] = None) -> Workload:
     """Workload k (1..5). `small=True` keeps the structure at a size the oracle
-    finishes in seconds (several ART blocks, ragged tails, paged tables)."""
+    finishes in seconds (several ART blocks, ragged tails, paged tables).
+    `batch` replaces the batch of a full-size config 2..5 (same shapes and
+    seeds otherwise; for smaller profiler captures of the same kernel); the
+    workload name then carries the new batch."""
     e = 1e-3 if eps is None else eps
     p = 2 if patience is None else patience
+    if batch is not None and (small or k == 1 or batch < 1):
+        raise ValueError("a batch override applies to the full-size configs 2..5")
+
+    def name(B0, B):
+        n = CONFIG_NAMES[k] + ("-small" if small else "")
+        return n if batch is None else n.replace(f"-b{B0}-", f"-b{B}-")
+
     if k == 1:
         return build(CONFIG_NAMES[1], seed=1, dtype="f32", batch=1, num_q_heads=1, num_kv_heads=1,
                      head_dim=64, page_size=64, block_size=64, seq_lens=[1024], paged="identity",
                      order=None, eps_mag=e, eps_dir=e, patience=p, threads=threads)
     if k == 2:
-        B, N = (2, 2000) if small else (16, 32768)
-        return build(CONFIG_NAMES[2] + ("-small" if small else ""), seed=2, dtype="bf16", batch=B,
+        B, N = (2, 2000) if small else (batch or 16, 32768)
+        return build(name(16, B), seed=2, dtype="bf16", batch=B,
                      num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=64, block_size=64,
                      seq_lens=[N] * B, paged="identity", plant=True, order="sink_recent",
                      eps_mag=e, eps_dir=e, patience=p, threads=threads)
     if k == 3:
-        B, N = (3, 1000) if small else (128, 8192)
-        return build(CONFIG_NAMES[3] + ("-small" if small else ""), seed=3, dtype="bf16", batch=B,
+        B, N = (3, 1000) if small else (batch or 128, 8192)
+        return build(name(128, B), seed=3, dtype="bf16", batch=B,
                      num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, block_size=64,
                      seq_lens=[N] * B, paged="permuted", plant=True, order="sink_recent",
                      eps_mag=e, eps_dir=e, patience=p, threads=threads)
@@ -347,15 +357,15 @@ def config(k: int, *, small: bool = False, eps: Optional[float] = None, patience
             B = 4
             lens = rs.integers(64, 3000, size=B, endpoint=True)
         else:
-            B = 64
+            B = batch or 64
             lens = rs.integers(1024, 65536, size=B, endpoint=True)
-        return build(CONFIG_NAMES[4] + ("-small" if small else ""), seed=4, dtype="bf16", batch=B,
+        return build(name(64, B), seed=4, dtype="bf16", batch=B,
                      num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, block_size=64,
                      seq_lens=lens, paged="permuted", v_boost_frac=0.05, v_boost=8.0,
                      order="sink_recent", eps_mag=e, eps_dir=e, patience=p, threads=threads)
     if k == 5:
-        B, N = (2, 4096) if small else (4, 131072)
-        return build(CONFIG_NAMES[5] + ("-small" if small else ""), seed=5, dtype="bf16", batch=B,
+        B, N = (2, 4096) if small else (batch or 4, 131072)
+        return build(name(4, B), seed=5, dtype="bf16", batch=B,
                      num_q_heads=28, num_kv_heads=4, head_dim=128, page_size=64, block_size=64,
                      seq_lens=[N] * B, paged="identity", plant=True,
                      selection=dict(top_frac=0.25, last=8), eps_mag=e, eps_dir=e, patience=p,
