@@ -222,6 +222,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) accesses.
+// two bf16 products, round to nearest
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

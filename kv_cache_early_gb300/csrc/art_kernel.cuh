@@ -67,6 +67,14 @@ struct Cfg {
     // record buffers: a group publishes entry u after the decision on u - 2 NG, which the
     // statistics warp may send before it has read u - 2 NG's partials
     static constexpr int NB = TC ? 4 * NG : 2;
+    // four tensor-core groups split the head dims between the warps of a group
+    // (fewer registers per warp); one or two groups, and the fp32 warps, split the keys
+    static constexpr bool DS = TC && NG == 4;
+    // rows of block partials per record: with the dims split each probe column has
+    // one writer; with the keys split, one row set per warp
+    static constexpr int RGW = DS ? 1 : GW;
+    static constexpr int DW = D / GW;            // tensor-core path: head dims per consumer warp
+    static constexpr int MT = DW / 16;           // ... and its O^T m-tiles
     static constexpr int THREADS = (NWC + 2) * 32;
     static constexpr int GQ = G;                 // query heads per KV head
     static constexpr int ELT = E::kBytes;
@@ -95,7 +103,8 @@ struct Cfg {
     // 8-wide tile and the low parts in columns 4-7, one mma per m-tile
     static constexpr bool SPLITN = TC && G <= 4;
     static constexpr int PRW = TC ? (SPLITN ? 2 : 1) : RPW;  // probe partial rows per warp
-    static constexpr int PART_F = NB * GW * PRW * PST;
+    static constexpr int PART_F = NB * RGW * PRW * PST;
+    static constexpr int XBW = SPLITN ? 2 : 4;   // words of a lane's P^T fragment
     static constexpr int KS = D / 16;            // tensor-core k-steps (QK) and m-tiles (PV)
     static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
     static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
@@ -108,16 +117,18 @@ struct SlotMeta {
     int item, pos, n, c, nvalid, kind, b, g, has0, pad0, pad1, pad2;
 };
 
+constexpr int kMaxNB = 16;  // record buffers at most (4 per consumer group)
+
 struct Ctrl {
-    int dec[8];
+    int dec[kMaxNB];
     int stop_item;
     int abort;
     int pad0, pad1;
-    SlotMeta info[8];  // item and position of each published record
+    SlotMeta info[kMaxNB];  // item and position of each published record
 };
 
 struct Layout {
-    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, sh, ptab, ctrl, total;
+    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, xb, xm, xl, sh, ptab, ctrl, total;
 };
 
 template <class C>
@@ -131,22 +142,30 @@ __host__ __device__ inline Layout make_layout(int stages) {
     L.bars = o;
     o += (size_t)(2 * stages + 2 * C::NB + 1) * sizeof(uint64_t);
     o = align_up(o, 16);
-    L.part = o;  // [NB][GW][PRW][PST] probe partial rows
+    L.part = o;  // [NB][RGW][PRW][PST] probe partial rows
     o += (size_t)C::PART_F * sizeof(float);
-    L.plb = o;  // [NB][GW][G] per-warp block sums
-    o += (size_t)C::NB * C::GW * G * sizeof(float);
-    L.pmb = o;  // [NB][GW][G] per-warp block maxima
-    o += (size_t)C::NB * C::GW * G * sizeof(float);
+    L.plb = o;  // [NB][RGW][G] block sums
+    o += (size_t)C::NB * C::RGW * G * sizeof(float);
+    L.pmb = o;  // [NB][RGW][G] block maxima
+    o += (size_t)C::NB * C::RGW * G * sizeof(float);
     L.wmax = o;  // [2][NWC][8] per-warp maxima of the block being processed (by block parity)
     o += (size_t)2 * C::NWC * 8 * sizeof(float);
     L.scr = o;  // [NWC][G][RW] scores, then weights
     o += (size_t)C::NWC * G * C::RW * sizeof(float);
     o = align_up(o, 16);
-    L.eacc = o;  // per consumer warp: [G][D] output sums, then [G] weight sums, then [G] maxima
-    o += (size_t)C::NWC * (G * C::DD + 2 * G) * sizeof(float);
+    L.eacc = o;  // per consumer warp (fp32) or group (tensor cores, 2+ groups): [G][D] output sums,
+                 // then [G] weight sums, then [G] maxima
+    o += (size_t)(C::DS ? C::NG : C::NWC) * (G * C::DD + 2 * G) * sizeof(float);
     o = align_up(o, 1024);
     L.qt = o;  // tensor-core path, per group: the item's queries, 8 rows (heads past G zero), 128B-swizzled
     o += C::TC ? (size_t)C::NG * 8 * C::ROWB : 0;
+    o = align_up(o, 16);
+    L.xb = o;  // dims split, per group and block parity: each warp's P^T fragments
+    o += C::DS ? (size_t)C::NG * 2 * C::GW * 32 * C::XBW * sizeof(uint32_t) : 0;
+    L.xm = o;  // ... [8 heads][GW] each warp's block max (a power-of-two exponent)
+    o += C::DS ? (size_t)C::NG * 2 * 8 * C::GW * sizeof(float) : 0;
+    L.xl = o;  // ... [8 heads][GW] each warp's weight sum relative to that max
+    o += C::DS ? (size_t)C::NG * 2 * 8 * C::GW * sizeof(float) : 0;
     o = align_up(o, 16);
     L.sh = o;  // [3][G] statistics warp scratch
     o += (size_t)3 * G * sizeof(float);
@@ -291,6 +310,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
         const char* kbase = static_cast<const char*>(p.k);
         const char* vbase = static_cast<const char*>(p.v);
         bool item_done = false;
+        int nis = 0;  // block entries issued for this item
         for (int base = 0; base < n && !item_done; base += 32) {
             // each lane resolves one listed position
             const int pos = base + lane;
@@ -337,6 +357,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                 if (badj) {
                     if (lane == 0) atomicOr(&p.hdr->status, ART_STATUS_BAD_PAGE);
                     if (!(ok = emit(kSlotFail, item, b, g))) break;
+                    nis = C::NG;  // every group got an entry of the item
                     item_done = true;
                     break;
                 }
@@ -396,11 +417,15 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                 }
                 __syncwarp();
                 advance();
+                ++nis;
             }
             if (!ok) break;
         }
         if (!ok) break;
-        if (C::NG > 1 && n == 1 && !(ok = emit1(kSlotPad, item, b, g, 1, 1))) break;
+        // every consumer group takes part in the item (its end is merged jointly):
+        // pads for the groups that got no block of it (short lists, early stops)
+        for (int k = nis; k < C::NG && ok; ++k) ok = emit1(kSlotPad, item, b, g, k, max(n, k + 1));
+        if (!ok) break;
     }
 
     if (!ok) {
@@ -425,7 +450,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
                           uint64_t* part_full, uint64_t* dec_bar, Ctrl* ctrl) {
     constexpr int G = C::GQ;
     constexpr int SPL = C::SPL;
-    constexpr int NP = C::GW * C::PRW;  // partial rows per record
+    constexpr int NP = C::RGW * C::PRW;  // partial rows per record
     constexpr int NB = C::NB;
     (void)sh;
     const int lane = threadIdx.x & 31;
@@ -496,24 +521,25 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         // block max and sum of this lane's head over the consumer warps (each warp
         // used its own max), new running max and sum, and the factor that moves
         // the probe: delta = cf * (PV_probe - l_blk * x)
-        float sw[C::GW];
+        constexpr int RGW = C::RGW;
+        float sw[RGW];
         float mbk = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::GW; ++w) {
-            sw[w] = pmb[(vb * C::GW + w) * G + hme];
+        for (int w = 0; w < RGW; ++w) {
+            sw[w] = pmb[(vb * RGW + w) * G + hme];
             mbk = fmaxf(mbk, sw[w]);
         }
         float lb = 0.f;
 #pragma unroll
-        for (int w = 0; w < C::GW; ++w) {
-            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a warp without valid keys adds nothing
-            lb = fmaf(sw[w], plb[(vb * C::GW + w) * G + hme], lb);
+        for (int w = 0; w < RGW; ++w) {
+            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a row set without valid keys adds nothing
+            lb = fmaf(sw[w], plb[(vb * RGW + w) * G + hme], lb);
         }
         const float Mn = fmaxf(M, mbk);
         const float a = exp2f(M - Mn);
         const float bw = exp2f(mbk - Mn);
         const float Ln = fmaf(a, Lsum, bw * lb);
-        const float cf = __fdividef(bw, Ln);  // Ln >= 1: the block's largest weight is 1 after rescaling
+        const float cf = __fdividef(bw, Ln);  // Ln >= 1/2: the block's largest weight is at least 1/2
         M = Mn;
         Lsum = Ln;
         const float* pp = part + (size_t)vb * NP * C::PST;
@@ -522,7 +548,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         for (int j = 0; j < SPL; ++j) {
             float pb = 0.f;
 #pragma unroll
-            for (int w = 0; w < C::GW; ++w) {
+            for (int w = 0; w < RGW; ++w) {
                 float pw = 0.f;
 #pragma unroll
                 for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
@@ -1162,6 +1188,12 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
 
     for (;;) {
         const int slot = u % p.stages;
+        if (NG > 1 && u >= p.stages) {
+            // the slot's previous entry belongs to another group and its copies may land
+            // after this group's own earlier entries: wait until it has been consumed, so
+            // that the parity test below cannot match that older fill
+            if (!wait_bounded(&empty[slot], (uint32_t)(u / p.stages - 1) & 1u, ctrl, p.hdr, 151 + gi)) return;
+        }
         if (!wait_bounded(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
         SlotMeta mt = meta[slot];
         if (mt.kind < 0 || mt.kind > kSlotPad ||
@@ -1340,9 +1372,493 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
 }
 
 // ---------------------------------------------------------------------------
+// tensor-core consumers (bf16), head dims split between the warps of a group
+//
+// A group of GW warps takes one 64-key block per ring entry. Warp wg computes
+// the scores of keys 16 wg .. 16 wg + 15 (S^T = K Q^T with mma.m16n8k16 from
+// the swizzled tiles) and its weights p = 2^(s - e) against its own max
+// rounded up to an integer e, so that two warps' weights differ by an exact
+// power of two. The warps exchange their weights (as P^T mma fragments),
+// exponents and weight sums through shared memory (one named barrier per
+// block); then warp wg computes O^T for head dims wg*DW .. (wg+1)*DW - 1 over
+// all 64 keys, each key chunk's fragment scaled to the group max exactly (a
+// bf16 multiply by a power of two). The weights are split into bf16 high +
+// low parts (p = hi + lo to ~2^-17); for G <= 4 the two parts share one 8-column
+// tile (columns 4-7 hold the low parts). Every warp therefore holds the
+// complete block result for its dims, and each probe column has one writer.
+//
+// Every entry gives the statistics warp one record (a computed block, or a
+// block / pad / failed / empty entry without data), in entry order. A group
+// publishes the record of its current entry, then waits for the decision on
+// its previous entry: "continue" folds that block into the group's
+// accumulators, "stop" folds it and ends the item, "discard" (a block past a
+// stop) ends the item without folding. A group also ends its item when its
+// next entry belongs to another item.
+// ---------------------------------------------------------------------------
+template <class C, bool kART>
+__device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta* meta, uint64_t* full,
+                            uint64_t* empty, uint64_t* part_full, uint64_t* dec_bar, uint64_t* cbar, const Layout& L,
+                            unsigned char* smem, const int* prank, Ctrl* ctrl) {
+    constexpr int G = C::GQ, D = C::DD, KS = C::KS, NWC = C::NWC, GW = C::GW, NG = C::NG, NB = C::NB;
+    constexpr int DW = C::DW, MT = C::MT, XBW = C::XBW;
+    using E = typename C::E;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = w / GW, wg = w % GW;  // group, warp within the group
+    const int grp = lane >> 2, tig = lane & 3;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    const bool v0 = h0 < G, v1 = h1 < G;  // the score columns of this lane hold real heads
+    // the O^T columns of this lane: heads (q0, q1); with the split tile, lanes with
+    // tig >= 2 hold the low parts of heads 2 tig - 4, 2 tig - 3
+    constexpr bool SPLITN = C::SPLITN;
+    const bool lo_lane = SPLITN && tig >= 2;
+    const int q0 = lo_lane ? h0 - 4 : h0, q1 = q0 + 1;
+    const bool u0 = q0 < G, u1 = q1 < G;                  // columns that belong to a real head
+    const bool w0 = u0 && !lo_lane, w1 = u1 && !lo_lane;  // ... and are written by this lane
+    // the head of this lane's P^T fragment column (column grp)
+    const int hb = (SPLITN && grp >= 4) ? grp - 4 : grp;
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    float* plb = reinterpret_cast<float*>(smem + L.plb);
+    float* pmb = reinterpret_cast<float*>(smem + L.pmb);
+    float* eacc = reinterpret_cast<float*>(smem + L.eacc);
+    uint32_t* xb = reinterpret_cast<uint32_t*>(smem + L.xb) + (size_t)gi * 2 * GW * 32 * XBW;
+    float* xm = reinterpret_cast<float*>(smem + L.xm) + (size_t)gi * 2 * 8 * GW;
+    float* xl = reinterpret_cast<float*>(smem + L.xl) + (size_t)gi * 2 * 8 * GW;
+    unsigned char* sQt = smem + L.qt + (size_t)gi * 8 * C::ROWB;
+    const uint32_t qtbase = smem_addr(sQt);
+    const float scale = 1.4426950408889634f / sqrtf((float)D);
+    const int ctid = threadIdx.x;   // 0 .. NWC*32-1
+    const int gtid = ctid % (GW * 32);
+    const int gbar = 1 + gi;        // named barrier of the group
+    // this lane's O^T rows are d = wg DW + 16 mt + 8 r + grp; bit 2 mt + r marks a probe
+    // column, byte 2 mt + r of prk holds its rank among the probe columns
+    uint32_t pbits = 0, prk = 0;
+    static_assert(2 * MT <= 4, "probe ranks of a lane fit one word");
+    if (kART) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int rk = prank[wg * DW + 16 * mt + 8 * r + grp];
+                if (rk >= 0) {
+                    pbits |= 1u << (2 * mt + r);
+                    prk |= (uint32_t)rk << (8 * (2 * mt + r));
+                }
+            }
+    }
+    const int mi = lane >> 3, lr = lane & 7;
+    const int keyK = wg * 16 + (mi & 1) * 8 + lr;  // K rows for the S^T A fragments
+    const int chK = mi >> 1;
+    const int keyV = (mi >> 1) * 8 + lr;           // V rows (within a 16-key chunk) for the O^T A fragments
+    const int chV = mi & 1;
+    auto sw = [](uint32_t base, int row, int chunk) -> uint32_t {
+        return base + (uint32_t)((chunk >> 3) * (kBK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    };
+
+    float acc[MT][4], tN[MT][4], tP[MT][4];
+    float mrun[2], lrun[2], mbN[2], lbN[2], mbP[2], lbP[2];
+    auto reset = [&]() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) { mrun[j] = -INFINITY; lrun[j] = 0.f; }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
+    };
+    reset();
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tN[mt][c] = tP[mt][c] = 0.f;
+    mbN[0] = mbN[1] = mbP[0] = mbP[1] = lbN[0] = lbN[1] = lbP[0] = lbP[1] = 0.f;
+
+    int u = gi;            // this group's current ring entry (= its record number)
+    int xpar = 0;          // exchange buffer of the next computed block
+    uint32_t cbph = 0;     // phase of the all-consumer barrier
+    int cur_item = -1, curb = 0, curg = 0;  // the item held in this group's accumulators
+    int stopped_item = -1;                  // the last item this group ended
+    bool pending = false, pcomp = false;    // previous entry awaiting its decision; computed?
+    int uP = 0, itemP = -1, posP = 0, nP = 0;
+
+    auto cbar_sync = [&]() -> bool {
+        __syncwarp();
+        mbar_arrive_if(lane == 0, cbar);
+        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr, 111 + gi);
+        cbph ^= 1u;
+        return r;
+    };
+    auto out_index = [&](int b, int g, int h, int col) -> size_t {
+        return ((size_t)b * p.Hq + (size_t)g * G + h) * D + col;
+    };
+    auto wait_dec = [&](int rec) -> int {
+        if (!wait_bounded(&dec_bar[rec % NB], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 121 + gi)) return -1;
+        return ctrl->dec[rec % NB];
+    };
+    auto fold = [&](const float (&t)[MT][4], const float* mb, const float* lb) {
+        float a[2], bb[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const bool none = mb[j] == -INFINITY;  // a head beyond G, or no valid key: keep the state
+            const float mn = none ? mrun[j] : fmaxf(mrun[j], mb[j]);
+            a[j] = none ? 1.f : exp2f(mrun[j] - mn);
+            bb[j] = none ? 0.f : exp2f(mb[j] - mn);
+            lrun[j] = none ? lrun[j] : a[j] * lrun[j] + bb[j] * lb[j];
+            mrun[j] = mn;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][c] = a[c & 1] * acc[mt][c] + bb[c & 1] * t[mt][c];
+    };
+    // write O = sum / weight sum for this warp's dims; with several groups, merge the
+    // groups' partials (each has its own running maxima) through shared memory first
+    auto finalize = [&]() -> bool {
+        if constexpr (SPLITN) {
+            // high + low parts (both lanes carry the same running max and sum)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[mt][c] += __shfl_xor_sync(0xffffffffu, acc[mt][c], 2);
+        }
+        const int ob = curb, og = curg;  // every group holds the same item
+        const bool okbg = ob >= 0 && ob < p.B && og >= 0 && og < p.Hkv;
+        if constexpr (NG == 1) {
+            if (!okbg) {
+                if (lane == 0) record_check(p.hdr, 3, ob, og, u);
+                return true;
+            }
+            const float r0 = 1.f / lrun[0], r1 = 1.f / lrun[1];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int d = wg * DW + 16 * mt + 8 * r + grp;
+                    if (w0) E::store(p.out, out_index(ob, og, q0, d), acc[mt][2 * r] * r0);
+                    if (w1) E::store(p.out, out_index(ob, og, q1, d), acc[mt][2 * r + 1] * r1);
+                }
+            return true;
+        } else {
+            float* mine = eacc + (size_t)gi * (G * D + 2 * G);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int d = wg * DW + 16 * mt + 8 * r + grp;
+                    if (w0) mine[q0 * D + d] = acc[mt][2 * r];
+                    if (w1) mine[q1 * D + d] = acc[mt][2 * r + 1];
+                }
+            if (wg == 0 && grp == 0) {
+                if (w0) { mine[G * D + q0] = lrun[0]; mine[G * D + G + q0] = mrun[0]; }
+                if (w1) { mine[G * D + q1] = lrun[1]; mine[G * D + G + q1] = mrun[1]; }
+            }
+            if (!cbar_sync()) return false;
+            if (!okbg && ctid == 0) record_check(p.hdr, 3, ob, og, u);
+            for (int idx = ctid; idx < G * D; idx += NWC * 32) {
+                const int h = idx / D;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) mx = fmaxf(mx, eacc[(size_t)gg * (G * D + 2 * G) + G * D + G + h]);
+                float num = 0.f, den = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) {
+                    const float* e = eacc + (size_t)gg * (G * D + 2 * G);
+                    const float mw = e[G * D + G + h];
+                    const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
+                    num += f * e[idx];
+                    den += f * e[G * D + h];
+                }
+                if (okbg) E::store(p.out, out_index(ob, og, h, idx - h * D), num / den);
+            }
+            return cbar_sync();
+        }
+    };
+    auto write_zero = [&](int b, int g) {
+        if (b < 0 || b >= p.B || g < 0 || g >= p.Hkv) {
+            if (gtid == 0) record_check(p.hdr, 4, b, g, u);
+            return;
+        }
+        for (int idx = gtid; idx < G * D; idx += GW * 32) E::store(p.out, out_index(b, g, idx / D, idx % D), 0.f);
+    };
+    // the record of entry u for the statistics warp
+    auto publish = [&](const SlotMeta& mt, int kind, bool computed) {
+        const int rb = u % NB;
+        if (kART) {
+            if (computed) {
+                // probe partial rows (high and low parts with the split tile); predicated
+                // stores, no divergent branches
+                float* pp = part + ((size_t)rb * C::PRW + (lo_lane ? 1 : 0)) * C::PST + q0;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const bool on = (pbits >> (2 * m + r)) & 1u;
+                        const int rank = (int)((prk >> (8 * (2 * m + r))) & 0xffu);
+                        float* dst = pp + rank * C::GP;
+                        if (G >= 2) st_shared_if(on && u1, dst, tN[m][2 * r], tN[m][2 * r + 1]);
+                        if (G % 2) st_shared_if(on && u0 && !u1, dst, tN[m][2 * r]);
+                    }
+                const bool lead = wg == 0 && grp == 0;
+                st_shared_if(lead && w0, &plb[rb * G + (w0 ? q0 : 0)], lbN[0]);
+                st_shared_if(lead && w1, &plb[rb * G + (w1 ? q1 : 0)], lbN[1]);
+                st_shared_if(lead && w0, &pmb[rb * G + (w0 ? q0 : 0)], mbN[0]);
+                st_shared_if(lead && w1, &pmb[rb * G + (w1 ? q1 : 0)], mbN[1]);
+            }
+            if (wg == 0 && lane == 0) {
+                SlotMeta& r = ctrl->info[rb];
+                r.kind = kind; r.item = mt.item; r.pos = mt.pos; r.n = mt.n; r.c = mt.c; r.has0 = mt.has0;
+            }
+            __syncwarp();
+            mbar_arrive_if(lane == 0, &part_full[rb]);
+        }
+    };
+    // bf16x2 multiplier 2^(e - emax) for a power-of-two exponent difference (0 below bf16 range)
+    auto pow2_bf16x2 = [](float e, float emax) -> uint32_t {
+        const float d = e - emax;  // an integer <= 0, or NaN / -inf
+        const int k = d >= -126.f ? (int)d : -1000;
+        const uint32_t bits = k >= -126 ? (uint32_t)(k + 127) << 7 : 0u;
+        return bits | (bits << 16);
+    };
+
+    for (;;) {
+        const int slot = u % p.stages;
+        if (NG > 1 && u >= p.stages) {
+            // the slot's previous entry belongs to another group and its copies may land
+            // after this group's own earlier entries: wait until it has been consumed, so
+            // that the parity test below cannot match that older fill
+            if (!wait_bounded(&empty[slot], (uint32_t)(u / p.stages - 1) & 1u, ctrl, p.hdr, 151 + gi)) return;
+        }
+        if (!wait_bounded(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
+        SlotMeta mt = meta[slot];
+        if (mt.kind < 0 || mt.kind > kSlotPad ||
+            (mt.kind == kSlotBlock && (mt.item < 0 || mt.item >= p.num_items || mt.nvalid < 1 || mt.nvalid > kBK ||
+                                       mt.pos < 0 || mt.pos >= mt.n || mt.b < 0 || mt.b >= p.B || mt.g < 0 ||
+                                       mt.g >= p.Hkv))) {
+            if (lane == 0) record_check(p.hdr, 5, u, mt.kind, mt.item);
+            mt.kind = kSlotPad;
+            mt.item = -2;
+        }
+        const bool is_data = mt.kind == kSlotBlock || mt.kind == kSlotPad;
+        const bool compute = mt.kind == kSlotBlock && mt.item != stopped_item;
+        if (compute) {
+            unsigned char* sK = ring + (size_t)slot * C::SLOT;
+            unsigned char* sV = sK + C::KVB;
+            if (mt.pos < NG) {
+                // the item's queries into this group's swizzled 8-row area (rows past G zero),
+                // once every warp of the group has finished the previous item's scores
+                named_bar_sync(gbar, GW * 32);
+                const unsigned char* sQ = sK + 2 * C::KVB;
+                constexpr int QCH = 8 * (C::ROWB / 16);
+                for (int i = gtid; i < QCH; i += GW * 32) {
+                    const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                    const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
+                }
+                named_bar_sync(gbar, GW * 32);
+            }
+            const int nvalid = mt.nvalid;
+            // ---- S^T for this warp's 16 keys (two independent accumulation chains);
+            // ldmatrix / mma.sync / movmatrix are warp-aligned: reconverge before them
+            float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kbase = smem_addr(sK), vbase = smem_addr(sV);
+            __syncwarp();
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t b00, b01, b10, b11;
+                {
+                    const int c = 4 * kp + mi;
+                    ldsm_x4(qtbase + (uint32_t)((c >> 3) * 1024 + lr * 128 + (((c & 7) ^ lr) << 4)), b00, b01, b10, b11);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ks = 2 * kp + h;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(sw(kbase, keyK, 2 * ks + chK), a0, a1, a2, a3);
+                    mma_bf16(h ? s4b : s4, a0, a1, a2, a3, h ? b10 : b00, h ? b11 : b01);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s4[c] += s4b[c];
+            const int k0 = wg * 16 + grp, k1 = k0 + 8;
+            float sc[4];
+            sc[0] = (k0 < nvalid && v0) ? s4[0] * scale : -INFINITY;
+            sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
+            sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
+            sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
+            // ---- this warp's max per head over its keys, rounded up to an integer exponent
+            float e0 = fmaxf(sc[0], sc[2]), e1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                e0 = fmaxf(e0, __shfl_xor_sync(0xffffffffu, e0, o));
+                e1 = fmaxf(e1, __shfl_xor_sync(0xffffffffu, e1, o));
+            }
+            e0 = ceilf(e0);
+            e1 = ceilf(e1);
+            float pw[4];
+            pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - e0);
+            pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - e1);
+            pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - e0);
+            pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - e1);
+            float l0 = pw[0] + pw[2], l1 = pw[1] + pw[3];
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+            // ---- P^T fragments of this warp's keys: hi and lo bf16 parts, transposed by movmatrix
+            uint32_t bf[XBW];
+            if constexpr (SPLITN) {
+                // low-part lanes take the weights of lane ^ 2
+                float px[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) px[c] = __shfl_xor_sync(0xffffffffu, pw[c], 2);
+                float t[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) t[c] = lo_lane ? px[c] : pw[c];
+                const uint32_t hA = pack_bf16(t[0], t[1]), hB = pack_bf16(t[2], t[3]);
+                const uint32_t lA = pack_bf16(t[0] - bf16_lo_f(hA), t[1] - bf16_hi_f(hA));
+                const uint32_t lB = pack_bf16(t[2] - bf16_lo_f(hB), t[3] - bf16_hi_f(hB));
+                __syncwarp();
+                bf[0] = movm_t(lo_lane ? lA : hA);
+                bf[1] = movm_t(lo_lane ? lB : hB);
+            } else {
+                const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
+                const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
+                const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
+                __syncwarp();
+                bf[0] = movm_t(hA); bf[1] = movm_t(hB); bf[2] = movm_t(lA); bf[3] = movm_t(lB);
+            }
+            // ---- publish fragments, exponents and sums to the group (every head column,
+            // -inf / 0 for heads past G), then wait for the other warps of the group
+            uint32_t* xbp = xb + (size_t)xpar * GW * 32 * XBW;
+            float* xmp = xm + xpar * 8 * GW;
+            float* xlp = xl + xpar * 8 * GW;
+            if constexpr (XBW == 2)
+                *reinterpret_cast<uint2*>(xbp + ((size_t)wg * 32 + lane) * 2) = make_uint2(bf[0], bf[1]);
+            else
+                *reinterpret_cast<uint4*>(xbp + ((size_t)wg * 32 + lane) * 4) = make_uint4(bf[0], bf[1], bf[2], bf[3]);
+            st_shared_if(grp == 0, &xmp[h0 * GW + wg], e0);
+            st_shared_if(grp == 0, &xmp[h1 * GW + wg], e1);
+            st_shared_if(grp == 0, &xlp[h0 * GW + wg], l0);
+            st_shared_if(grp == 0, &xlp[h1 * GW + wg], l1);
+            // ---- rows past the sequence end hold stale data: zero this warp's dims of them,
+            // so that 0 * V stays 0
+            if (nvalid < kBK) {
+                constexpr int CPR = DW / 8;  // 16-byte chunks of a row in this warp's dims
+                const int nchunks = (kBK - nvalid) * CPR;
+                for (int i = lane; i < nchunks; i += 32) {
+                    const int row = nvalid + i / CPR, c = wg * CPR + i % CPR;
+                    *reinterpret_cast<uint4*>(sV + (c >> 3) * (kBK * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            named_bar_sync(gbar, GW * 32);
+            // ---- the group's max exponent and weight sum per head
+            float emx[2], ebh = -INFINITY;
+            {
+                const float4 mq0 = *reinterpret_cast<const float4*>(xmp + (u0 ? q0 : 0) * GW);
+                const float4 mq1 = *reinterpret_cast<const float4*>(xmp + (u1 ? q1 : 0) * GW);
+                const float4 lq0 = *reinterpret_cast<const float4*>(xlp + (u0 ? q0 : 0) * GW);
+                const float4 lq1 = *reinterpret_cast<const float4*>(xlp + (u1 ? q1 : 0) * GW);
+                static_assert(GW == 4, "one float4 per head");
+                emx[0] = fmaxf(fmaxf(mq0.x, mq0.y), fmaxf(mq0.z, mq0.w));
+                emx[1] = fmaxf(fmaxf(mq1.x, mq1.y), fmaxf(mq1.z, mq1.w));
+                auto wsum = [](const float4& m, const float4& l, float mx) {
+                    float s = 0.f;
+                    s += m.x == -INFINITY ? 0.f : exp2f(m.x - mx) * l.x;
+                    s += m.y == -INFINITY ? 0.f : exp2f(m.y - mx) * l.y;
+                    s += m.z == -INFINITY ? 0.f : exp2f(m.z - mx) * l.z;
+                    s += m.w == -INFINITY ? 0.f : exp2f(m.w - mx) * l.w;
+                    return s;
+                };
+                mbN[0] = u0 ? emx[0] : -INFINITY;
+                mbN[1] = u1 ? emx[1] : -INFINITY;
+                lbN[0] = u0 && emx[0] != -INFINITY ? wsum(mq0, lq0, emx[0]) : 0.f;
+                lbN[1] = u1 && emx[1] != -INFINITY ? wsum(mq1, lq1, emx[1]) : 0.f;
+            }
+            const float4 mb4 = *reinterpret_cast<const float4*>(xmp + hb * GW);
+            ebh = fmaxf(fmaxf(mb4.x, mb4.y), fmaxf(mb4.z, mb4.w));
+            const float mbw[4] = {mb4.x, mb4.y, mb4.z, mb4.w};
+            // ---- O^T of this warp's dims over the block's 64 keys, chunk by chunk
+#pragma unroll
+            for (int m = 0; m < MT; ++m) tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < GW; ++c) {
+                uint32_t b[XBW];
+                if constexpr (XBW == 2) {
+                    const uint2 t2 = *reinterpret_cast<const uint2*>(xbp + ((size_t)c * 32 + lane) * 2);
+                    b[0] = t2.x; b[1] = t2.y;
+                } else {
+                    const uint4 t4 = *reinterpret_cast<const uint4*>(xbp + ((size_t)c * 32 + lane) * 4);
+                    b[0] = t4.x; b[1] = t4.y; b[2] = t4.z; b[3] = t4.w;
+                }
+                const uint32_t sc2 = hb < G ? pow2_bf16x2(mbw[c], ebh) : 0u;
+#pragma unroll
+                for (int k = 0; k < XBW; ++k) b[k] = hmul2_bf16(b[k], sc2);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(sw(vbase, 16 * c + keyV, 2 * (wg * MT + m) + chV), a0, a1, a2, a3);
+                    mma_bf16(tN[m], a0, a1, a2, a3, b[0], b[1]);
+                    if constexpr (!SPLITN) mma_bf16(tN[m], a0, a1, a2, a3, b[2], b[3]);
+                }
+            }
+            xpar ^= 1;
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0 && mt.kind != kSlotEnd, &empty[slot]);  // the slot's data are no longer read
+
+        // ---- this entry's record, then the decision on the previous one
+        publish(mt, (mt.kind == kSlotBlock && !compute) ? kSlotPad : mt.kind, compute);
+        bool ended = false;
+        if (pending) {
+            int d;
+            if (kART) {
+                d = wait_dec(uP);
+                if (d < 0) return;
+            } else {
+                d = !pcomp ? kDiscard : (posP == nP - 1 ? kStop : kContinue);
+            }
+            if (pcomp && d != kDiscard) fold(tP, mbP, lbP);
+            ended = (d == kStop || d == kDiscard) && itemP == cur_item;
+            pending = false;
+        }
+        if (cur_item != -1 && (ended || mt.item != cur_item || !is_data)) {
+            if (!finalize()) return;
+            reset();
+            stopped_item = cur_item;
+            cur_item = -1;
+        }
+        if (mt.kind == kSlotEnd) return;
+        if (!is_data && mt.pos == 0) write_zero(mt.b, mt.g);
+        if (is_data && cur_item == -1 && mt.item != stopped_item) {
+            cur_item = mt.item;
+            curb = mt.b;
+            curg = mt.g;
+        }
+        // this entry waits for its decision until this group's next entry
+        pending = true;
+        pcomp = compute;
+        uP = u;
+        itemP = mt.item;
+        posP = mt.pos;
+        nP = mt.n;
+        if (compute) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tP[m][c] = tN[m][c];
+            mbP[0] = mbN[0]; mbP[1] = mbN[1]; lbP[0] = lbN[0]; lbP[1] = lbN[1];
+        }
+        u += NG;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-// one tensor-core group per CTA runs two CTAs per SM; two groups share one CTA per SM
+// tensor cores: one group per CTA runs two CTAs per SM; two or four groups one
 template <class C>
 struct MinBlocks {
     static constexpr int value = (C::TC && C::NG == 1) ? 2 : 1;
@@ -1428,7 +1944,10 @@ __global__ void __launch_bounds__(Cfg<kBF16, D, G, kNG>::THREADS, (MinBlocks<Cfg
                          reinterpret_cast<const float*>(smem + L.pmb), reinterpret_cast<float*>(smem + L.sh),
                          part_full, dec_bar, ctrl);
     } else if constexpr (C::TC) {
-        consumer_tc<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, prank, ctrl);
+        if constexpr (C::DS)
+            consumer_ds<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, prank, ctrl);
+        else
+            consumer_tc<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, prank, ctrl);
     } else {
         consumer_warps<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, pmask, pbase, ctrl);
     }
@@ -1481,8 +2000,9 @@ cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, Laun
     using C = Cfg<kBF16, D, G, kNG>;
     auto kern = art_decode_kernel<kBF16, D, G, kNG, kART>;
     cudaError_t e;
-    // two CTAs per SM only pay when there are items for both
-    const int want = (MinBlocks<C>::value > 1 && p.num_items > sms) ? 2 : 1;
+    // several CTAs per SM only pay when there are items for them
+    const int per_sm = (p.num_items + sms - 1) / sms;
+    const int want = MinBlocks<C>::value < per_sm ? MinBlocks<C>::value : per_sm;
     int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(want, smem_sm, smem_blk);
     if (stages == 0) stages = pick_stages<C>(1, smem_sm, smem_blk);
     if (stages == 0) return cudaErrorInvalidConfiguration;
@@ -1521,13 +2041,16 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
         return e;
     if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    // bf16: with fewer items than two per SM, two consumer groups per CTA split each
-    // item's blocks; otherwise one group per CTA and two CTAs per SM
+    // bf16: with at least two items per SM, one consumer group per CTA and three CTAs
+    // per SM; with fewer, several groups of one CTA take alternate blocks of an item
+    // (two groups and two CTAs per SM down to one item per SM, else four groups)
     const char* env = std::getenv("ART_GROUPS");
-    const int groups = env ? std::atoi(env) : (p.num_items < 2 * sms ? 2 : 1);
+    const int groups = env ? std::atoi(env) : (p.num_items >= 2 * sms ? 1 : p.num_items >= sms ? 2 : 4);
     if constexpr (kBF16) {
         if (groups == 2)
             return launch_variant<kBF16, D, G, 2, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+        if (groups == 4)
+            return launch_variant<kBF16, D, G, 4, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
     }
     return launch_variant<kBF16, D, G, 1, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
 }

@@ -215,3 +215,45 @@ def test_full_size_sampled(full_cache, k, eps, p):
     outd, _, st, _ = run_gpu(w, "dense", dev=dev)
     assert st == 0
     check_dense(w, outd, items=items, what=f"full dense config {k}")
+
+
+@pytest.mark.parametrize("groups", ["1", "2", "4"])
+@pytest.mark.parametrize("k", [2, 3, 4, 5])
+def test_consumer_group_variants(small, k, groups, monkeypatch):
+    """Each bf16 kernel variant (one, two or four consumer groups per CTA; the
+    library picks one from the item count, ART_GROUPS forces it) against the
+    oracle, ART and dense."""
+    monkeypatch.setenv("ART_GROUPS", groups)
+    w = small[k]
+    out, bu, st, dev = run_gpu(w, "art", 1e-2, 1e-2, 2)
+    assert st == 0
+    check_art(w, out, bu, 1e-2, 1e-2, 2, what=f"art config {k} groups {groups}")
+    out, bu, st, _ = run_gpu(w, "art", 0.0, 0.0, 1, dev=dev)
+    assert st == 0 and (bu == w.visit_lengths()).all()
+    out, _, st, _ = run_gpu(w, "dense", dev=dev)
+    assert st == 0
+    check_dense(w, out, what=f"dense config {k} groups {groups}")
+
+
+@pytest.mark.parametrize("groups", ["2", "4"])
+def test_many_short_items_multi_group(groups, monkeypatch):
+    """Hundreds of short items per call: with several consumer groups the ring
+    slots change hands between groups at every item, and blocks of different
+    groups land out of order. Repeated calls must all finish cleanly (status 0)
+    and match the oracle."""
+    monkeypatch.setenv("ART_GROUPS", groups)
+    rs = np.random.default_rng(77)
+    lens = rs.integers(1, 1500, size=64)
+    w = W.build("short-items", seed=61, dtype="bf16", batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                page_size=16, block_size=64, seq_lens=list(lens), paged="permuted", plant=True,
+                order="sink_recent")
+    items = np.sort(rs.choice(w.num_items, size=48, replace=False))
+    dev = None
+    for call in range(3):
+        out, bu, st, dev = run_gpu(w, "dense", dev=dev)
+        assert st == 0, f"dense call {call}: status {st}"
+        out, bu, st, dev = run_gpu(w, "art", 1e-2, 1e-2, 1, dev=dev)
+        assert st == 0, f"art call {call}: status {st}"
+    check_art(w, out, bu, 1e-2, 1e-2, 1, items=items, what=f"short items, groups {groups}")
+    out, _, st, _ = run_gpu(w, "dense", dev=dev)
+    check_dense(w, out, items=items, what=f"short items dense, groups {groups}")
