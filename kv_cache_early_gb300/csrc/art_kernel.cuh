@@ -65,11 +65,12 @@ struct Cfg {
     static constexpr int GW = TC ? 4 : 8;        // warps per consumer group
     static constexpr int NWC = NG * GW;          // consumer warps
     // record buffers: a group publishes entry u after the decision on u - 2 NG, which the
-    // statistics warp may send before it has read u - 2 NG's partials
-    static constexpr int NB = TC ? 4 * NG : 2;
+    // statistics warp may send before it has read u - 2 NG's partials, so NB > 2 NG; a
+    // multiple of NG keeps each buffer (and its decision word) with one group
+    static constexpr int NB = TC ? 3 * NG : 2;
     // four tensor-core groups split the head dims between the warps of a group
     // (fewer registers per warp); one or two groups, and the fp32 warps, split the keys
-    static constexpr bool DS = TC && NG == 4;
+    static constexpr bool DS = TC && NG >= 3;
     // rows of block partials per record: with the dims split each probe column has
     // one writer; with the keys split, one row set per warp
     static constexpr int RGW = DS ? 1 : GW;
@@ -105,6 +106,9 @@ struct Cfg {
     static constexpr int PRW = TC ? (SPLITN ? 2 : 1) : RPW;  // probe partial rows per warp
     static constexpr int PART_F = NB * RGW * PRW * PST;
     static constexpr int XBW = SPLITN ? 2 : 4;   // words of a lane's P^T fragment
+    // bytes of a group's exchange area (dims split); the item-end merge reuses it
+    static constexpr int XGB = (2 * GW * 32 * XBW + 2 * 2 * 8 * GW) * 4;
+    static_assert(!TC || NG < 3 || XGB >= (G * D + 2 * G) * 4, "merge area fits the exchange area");
     static constexpr int KS = D / 16;            // tensor-core k-steps (QK) and m-tiles (PV)
     static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
     static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
@@ -128,7 +132,7 @@ struct Ctrl {
 };
 
 struct Layout {
-    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, xb, xm, xl, sh, ptab, ctrl, total;
+    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, xb, sh, ptab, ctrl, total;
 };
 
 template <class C>
@@ -148,24 +152,22 @@ __host__ __device__ inline Layout make_layout(int stages) {
     o += (size_t)C::NB * C::RGW * G * sizeof(float);
     L.pmb = o;  // [NB][RGW][G] block maxima
     o += (size_t)C::NB * C::RGW * G * sizeof(float);
-    L.wmax = o;  // [2][NWC][8] per-warp maxima of the block being processed (by block parity)
-    o += (size_t)2 * C::NWC * 8 * sizeof(float);
-    L.scr = o;  // [NWC][G][RW] scores, then weights
-    o += (size_t)C::NWC * G * C::RW * sizeof(float);
+    L.wmax = o;  // fp32 path: [2][NWC][8] per-warp maxima of the block being processed (by block parity)
+    o += C::TC ? 0 : (size_t)2 * C::NWC * 8 * sizeof(float);
+    L.scr = o;  // fp32 path: [NWC][G][RW] scores, then weights
+    o += C::TC ? 0 : (size_t)C::NWC * G * C::RW * sizeof(float);
     o = align_up(o, 16);
-    L.eacc = o;  // per consumer warp (fp32) or group (tensor cores, 2+ groups): [G][D] output sums,
-                 // then [G] weight sums, then [G] maxima
-    o += (size_t)(C::DS ? C::NG : C::NWC) * (G * C::DD + 2 * G) * sizeof(float);
+    L.eacc = o;  // per consumer warp: [G][D] output sums, then [G] weight sums, then [G] maxima
+                 // (dims split: per group, in the group's exchange area, which is idle then)
+    o += C::DS ? 0 : (size_t)C::NWC * (G * C::DD + 2 * G) * sizeof(float);
     o = align_up(o, 1024);
     L.qt = o;  // tensor-core path, per group: the item's queries, 8 rows (heads past G zero), 128B-swizzled
     o += C::TC ? (size_t)C::NG * 8 * C::ROWB : 0;
     o = align_up(o, 16);
-    L.xb = o;  // dims split, per group and block parity: each warp's P^T fragments
-    o += C::DS ? (size_t)C::NG * 2 * C::GW * 32 * C::XBW * sizeof(uint32_t) : 0;
-    L.xm = o;  // ... [8 heads][GW] each warp's block max (a power-of-two exponent)
-    o += C::DS ? (size_t)C::NG * 2 * 8 * C::GW * sizeof(float) : 0;
-    L.xl = o;  // ... [8 heads][GW] each warp's weight sum relative to that max
-    o += C::DS ? (size_t)C::NG * 2 * 8 * C::GW * sizeof(float) : 0;
+    L.xb = o;  // dims split, per group: [2 block parities][GW warps][32 lanes] P^T fragments,
+               // then [2][8 heads][GW] block max exponents, then [2][8][GW] weight sums
+    o += C::DS ? (size_t)C::NG * C::XGB : 0;
+    if (C::DS) L.eacc = L.xb;
     o = align_up(o, 16);
     L.sh = o;  // [3][G] statistics warp scratch
     o += (size_t)3 * G * sizeof(float);
@@ -468,7 +470,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
     const int hme = lane % C::GP < G ? lane % C::GP : 0;
     float M = -INFINITY, Lsum = 0.f;
     float X[SPL];
-    float nprev = 0.f;  // |x_{i-1}|
+    float nprev = 0.f, rprev = 0.f;  // |x_{i-1}| and its reciprocal
     int counter = 0, seen0 = 0;
     int stopped_item = -1;
     auto reset = [&]() {
@@ -477,6 +479,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
 #pragma unroll
         for (int j = 0; j < SPL; ++j) X[j] = 0.f;
         nprev = 0.f;
+        rprev = 0.f;
         counter = 0;
         seen0 = 0;
     };
@@ -567,19 +570,21 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
             s2 += __shfl_xor_sync(0xffffffffu, s2, o);
             s3 += __shfl_xor_sync(0xffffffffu, s3, o);
         }
-        // |x_i| - |x_{i-1}| = (|x_i|^2 - |x_{i-1}|^2) / (|x_i| + |x_{i-1}|) with the
-        // difference of squares formed directly as 2 s2 + s1;
-        // 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2 = (s1 - 2 s2 dn / n_{i-1} + dn^2) / (2 |x_i|^2).
-        // Fast divisions (a few ulp): the results only meet the thresholds, whose
-        // decisions are exact up to a tie zone far wider than that.
+        // With S = |x_i| + |x_{i-1}| and T = |x_i|^2 - |x_{i-1}|^2 = 2 s2 + s1 (the difference
+        // of squares formed directly):
+        //   d_mag = |T| / (S |x_{i-1}|)
+        //   d_dir = 1 - cos = |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2
+        //         = (s1 - 2 s2 (T/S) / |x_{i-1}| + (T/S)^2) / (2 s3), clamped at 0.
+        // Both tests are taken multiplied through by their (positive) denominators, so
+        // no division sits on the chain; 1/|x_{i-1}| comes from the previous block.
         const float ni = sqrtf(s3);
-        const float dn = __fdividef(2.f * s2 + s1, ni + nprev);
-        const float rprev = __fdividef(1.f, nprev);
-        const float dmag = fabsf(dn) * rprev;
-        const float ddir = fmaxf(0.f, __fdividef(s1 - 2.f * s2 * (dn * rprev) + dn * dn, 2.f * s3));
-        const bool stable = pos >= 1 && nprev > 0.f && ni > 0.f && nprev < 1e30f && ni < 1e30f &&
-                            dmag < p.eps_mag && ddir < p.eps_dir;
+        const float S = ni + nprev, T = 2.f * s2 + s1;
+        const bool mag_ok = fabsf(T) * rprev < p.eps_mag * S;
+        const float Nd = fmaf(s1, S * S, fmaf(-2.f * s2 * T, S * rprev, T * T));
+        const bool dir_ok = fmaxf(0.f, Nd) < 2.f * p.eps_dir * s3 * (S * S);
+        const bool stable = pos >= 1 && nprev > 0.f && ni > 0.f && nprev < 1e30f && ni < 1e30f && mag_ok && dir_ok;
         nprev = ni;
+        rprev = __fdividef(1.f, ni);  // a few ulp; the next block's tests only
         counter = stable ? counter + 1 : 0;
         const bool stop = last || (may_stop && counter >= p.patience);
         if (stop) {
@@ -1420,9 +1425,9 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
     float* plb = reinterpret_cast<float*>(smem + L.plb);
     float* pmb = reinterpret_cast<float*>(smem + L.pmb);
     float* eacc = reinterpret_cast<float*>(smem + L.eacc);
-    uint32_t* xb = reinterpret_cast<uint32_t*>(smem + L.xb) + (size_t)gi * 2 * GW * 32 * XBW;
-    float* xm = reinterpret_cast<float*>(smem + L.xm) + (size_t)gi * 2 * 8 * GW;
-    float* xl = reinterpret_cast<float*>(smem + L.xl) + (size_t)gi * 2 * 8 * GW;
+    uint32_t* xb = reinterpret_cast<uint32_t*>(smem + L.xb + (size_t)gi * C::XGB);
+    float* xm = reinterpret_cast<float*>(xb + 2 * GW * 32 * XBW);
+    float* xl = xm + 2 * 8 * GW;
     unsigned char* sQt = smem + L.qt + (size_t)gi * 8 * C::ROWB;
     const uint32_t qtbase = smem_addr(sQt);
     const float scale = 1.4426950408889634f / sqrtf((float)D);
@@ -1537,7 +1542,7 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
                 }
             return true;
         } else {
-            float* mine = eacc + (size_t)gi * (G * D + 2 * G);
+            float* mine = eacc + (size_t)gi * (C::XGB / 4);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -1556,11 +1561,11 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
                 const int h = idx / D;
                 float mx = -INFINITY;
 #pragma unroll
-                for (int gg = 0; gg < NG; ++gg) mx = fmaxf(mx, eacc[(size_t)gg * (G * D + 2 * G) + G * D + G + h]);
+                for (int gg = 0; gg < NG; ++gg) mx = fmaxf(mx, eacc[(size_t)gg * (C::XGB / 4) + G * D + G + h]);
                 float num = 0.f, den = 0.f;
 #pragma unroll
                 for (int gg = 0; gg < NG; ++gg) {
-                    const float* e = eacc + (size_t)gg * (G * D + 2 * G);
+                    const float* e = eacc + (size_t)gg * (C::XGB / 4);
                     const float mw = e[G * D + G + h];
                     const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
                     num += f * e[idx];
@@ -2041,14 +2046,16 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
         return e;
     if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    // bf16: with at least two items per SM, one consumer group per CTA and three CTAs
-    // per SM; with fewer, several groups of one CTA take alternate blocks of an item
-    // (two groups and two CTAs per SM down to one item per SM, else four groups)
+    // bf16: with at least two items per SM, one consumer group per CTA and two CTAs per
+    // SM; with fewer, several groups of one CTA take alternate blocks of an item (two
+    // groups down to one item per SM, else three). ART_GROUPS (1..4) overrides the choice.
     const char* env = std::getenv("ART_GROUPS");
-    const int groups = env ? std::atoi(env) : (p.num_items >= 2 * sms ? 1 : p.num_items >= sms ? 2 : 4);
+    const int groups = env ? std::atoi(env) : (p.num_items >= 2 * sms ? 1 : p.num_items >= sms ? 2 : 3);
     if constexpr (kBF16) {
         if (groups == 2)
             return launch_variant<kBF16, D, G, 2, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+        if (groups == 3)
+            return launch_variant<kBF16, D, G, 3, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
         if (groups == 4)
             return launch_variant<kBF16, D, G, 4, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
     }

@@ -217,10 +217,10 @@ def test_full_size_sampled(full_cache, k, eps, p):
     check_dense(w, outd, items=items, what=f"full dense config {k}")
 
 
-@pytest.mark.parametrize("groups", ["1", "2", "4"])
+@pytest.mark.parametrize("groups", ["1", "2", "3", "4"])
 @pytest.mark.parametrize("k", [2, 3, 4, 5])
 def test_consumer_group_variants(small, k, groups, monkeypatch):
-    """Each bf16 kernel variant (one, two or four consumer groups per CTA; the
+    """Each bf16 kernel variant (one to four consumer groups per CTA; the
     library picks one from the item count, ART_GROUPS forces it) against the
     oracle, ART and dense."""
     monkeypatch.setenv("ART_GROUPS", groups)
@@ -235,7 +235,7 @@ def test_consumer_group_variants(small, k, groups, monkeypatch):
     check_dense(w, out, what=f"dense config {k} groups {groups}")
 
 
-@pytest.mark.parametrize("groups", ["2", "4"])
+@pytest.mark.parametrize("groups", ["2", "3", "4"])
 def test_many_short_items_multi_group(groups, monkeypatch):
     """Hundreds of short items per call: with several consumer groups the ring
     slots change hands between groups at every item, and blocks of different
