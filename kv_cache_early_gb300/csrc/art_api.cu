@@ -270,6 +270,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     p.eps_mag = eps_mag;
     p.eps_dir = eps_dir;
     p.patience = patience;
+    p.tma3d = 0;
     if (t_events.start && (e = cudaEventRecord(t_events.start, st)) != cudaSuccess) return cuda_fail(e);
     e = dispatch<kART>(s, p, st, env_stages(), li);
     if (e != cudaSuccess) return cuda_fail(e);

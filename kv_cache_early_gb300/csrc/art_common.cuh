@@ -65,6 +65,7 @@ struct Params {
     const int32_t* order;
     const ItemInfo* info;
     int B, Hq, Hkv, Ps, max_pages, max_visit, m, num_pages, num_items, stages;
+    int tma3d;  // tensor-core path: one 3-D copy per page (else one 2-D copy per 128-byte column half)
     float eps_mag, eps_dir;
     int patience;
 };
@@ -140,6 +141,19 @@ __device__ __forceinline__ void st_shared_if(bool pred, float* p, float x, float
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+}
+
+// Non-blocking test of a phase (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -221,7 +235,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
         : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // two bf16 products, round to nearest
 __device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -229,6 +250,7 @@ __device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
     return d;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -218,6 +218,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctrl* ctrl, WsHeader* hdr,
                                              int where = 0) {
     constexpr uint32_t kSleepNs = 200000;  // upper bound of one sleep; the limit is checked between sleeps
+    // a phase that has completed already costs one test, not a (slower) suspending wait
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
@@ -376,22 +378,27 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                 }
                 __syncwarp();
                 if constexpr (C::TC) {
-                    // 128-byte column boxes of each page, written 128B-swizzled by the tensor maps
+                    // each page's rows land as [column half][rows] (128-byte rows, 128B-swizzled),
+                    // pages one after another; one 3-D copy per page, or one 2-D copy per half
                     constexpr int NH = C::ROWB / 128;
                     const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
-                    const int nbox = 2 * npj * NH;
+                    const int nop = p.tma3d ? npj : npj * NH;  // copies of K (and of V)
+                    const int nbox = 2 * nop;
                     for (int t = lane; t < nbox + (with_q ? 1 : 0); t += 32) {
                         if (t < nbox) {
-                            const int kv = t / (npj * NH);
-                            const int rem = t - kv * npj * NH;
-                            const int k = rem / NH, hf = rem - (rem / NH) * NH;
+                            const int kv = t / nop;
+                            const int rem = t - kv * nop;
+                            const int k = p.tma3d ? rem : rem / NH, hf = p.tma3d ? 0 : rem - (rem / NH) * NH;
                             int pk = 0;
 #pragma unroll
                             for (int u = 0; u < 8; ++u)
                                 if (u == k) pk = pgj[u];
                             const int y = (pk * p.Hkv + g) * p.Ps + r0j;
-                            unsigned char* d = dst + kv * C::KVB + hf * (kBK * 128) + k * page_rows * 128;
-                            tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
+                            unsigned char* d = dst + kv * C::KVB + (k * NH + hf) * page_rows * 128;
+                            if (p.tma3d)
+                                tma_load_3d(d, kv ? tv : tk, 0, y, 0, &full[slot]);
+                            else
+                                tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
                         } else {
                             const char* src =
                                 static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
@@ -1049,8 +1056,15 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
     const int chK = mi >> 1;
     const int keyV = wg * 16 + (mi >> 1) * 8 + lr;  // V rows for the O^T A fragments
     const int chV = mi & 1;
-    auto sw = [](uint32_t base, int row, int chunk) -> uint32_t {
-        return base + (uint32_t)((chunk >> 3) * (kBK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    // K / V tiles: pages of PR rows one after another, each as [column half][PR rows][128 B],
+    // 16-byte chunks of a row XOR-swizzled by the row (128B swizzle)
+    const int PR = p.Ps < kBK ? p.Ps : kBK;
+    const int lpr = 31 - __clz(PR);
+    auto rowoff = [=](int row) -> uint32_t {
+        return (uint32_t)(((row >> lpr) * (C::ROWB / 128) * PR + (row & (PR - 1))) * 128);
+    };
+    auto sw = [=](uint32_t base, int row, int chunk) -> uint32_t {
+        return base + rowoff(row) + (uint32_t)((chunk >> 3) * PR * 128 + (((chunk & 7) ^ (row & 7)) << 4));
     };
 
     float acc[KS][4], tN[KS][4], tP[KS][4];
@@ -1310,7 +1324,7 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
                 const int nchunks = (wg * 16 + 16 - r0) * (C::ROWB / 16);
                 for (int i = lane; i < nchunks; i += 32) {
                     const int row = r0 + i / (C::ROWB / 16), c = i % (C::ROWB / 16);
-                    *reinterpret_cast<uint4*>(sV + (c >> 3) * (kBK * 128) + row * 128 + (c & 7) * 16) =
+                    *reinterpret_cast<uint4*>(sV + rowoff(row) + (c >> 3) * PR * 128 + (c & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -1455,8 +1469,15 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
     const int chK = mi >> 1;
     const int keyV = (mi >> 1) * 8 + lr;           // V rows (within a 16-key chunk) for the O^T A fragments
     const int chV = mi & 1;
-    auto sw = [](uint32_t base, int row, int chunk) -> uint32_t {
-        return base + (uint32_t)((chunk >> 3) * (kBK * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    // K / V tiles: pages of PR rows one after another, each as [column half][PR rows][128 B],
+    // 16-byte chunks of a row XOR-swizzled by the row (128B swizzle)
+    const int PR = p.Ps < kBK ? p.Ps : kBK;
+    const int lpr = 31 - __clz(PR);
+    auto rowoff = [=](int row) -> uint32_t {
+        return (uint32_t)(((row >> lpr) * (C::ROWB / 128) * PR + (row & (PR - 1))) * 128);
+    };
+    auto sw = [=](uint32_t base, int row, int chunk) -> uint32_t {
+        return base + rowoff(row) + (uint32_t)((chunk >> 3) * PR * 128 + (((chunk & 7) ^ (row & 7)) << 4));
     };
 
     float acc[MT][4], tN[MT][4], tP[MT][4];
@@ -1752,7 +1773,7 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
                 const int nchunks = (kBK - nvalid) * CPR;
                 for (int i = lane; i < nchunks; i += 32) {
                     const int row = nvalid + i / CPR, c = wg * CPR + i % CPR;
-                    *reinterpret_cast<uint4*>(sV + (c >> 3) * (kBK * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+                    *reinterpret_cast<uint4*>(sV + rowoff(row) + (c >> 3) * PR * 128 + (((c & 7) ^ (row & 7)) << 4)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -1986,6 +2007,22 @@ inline EncodeTiledFn encode_tiled_fn() {
 
 // A 2-D bf16 view [rows = pages * Hkv * page_size][D] of a cache, read in
 // boxes of 64 columns (128 bytes) by min(page_size, 64) rows, 128B-swizzled.
+// A 3-D bf16 view {64 columns, rows, column halves} of the same cache (strides: a row
+// D * 2 bytes, a half 128 bytes), read one page of rows (both halves) per copy: the box
+// lands as [half][rows][64 columns], 128B-swizzled.
+inline cudaError_t make_cache_map3(CUtensorMap* m, const void* base, long long rows, int D, int Ps) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(Ps < kBK ? Ps : kBK), (cuuint32_t)(D / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 inline cudaError_t make_cache_map(CUtensorMap* m, const void* base, long long rows, int D, int Ps) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -2024,8 +2061,14 @@ cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, Laun
     if (C::TC) {
         const long long rows = (long long)p.num_pages * p.Hkv * p.Ps;
         if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
-        if ((e = make_cache_map(&tk, p.k, rows, D, p.Ps)) != cudaSuccess) return e;
-        if ((e = make_cache_map(&tv, p.v, rows, D, p.Ps)) != cudaSuccess) return e;
+        // one copy per page where the driver takes the 3-D view, else one per column half
+        const char* env3 = std::getenv("ART_TMA3D");
+        p.tma3d = (!env3 || std::atoi(env3) != 0) && make_cache_map3(&tk, p.k, rows, D, p.Ps) == cudaSuccess &&
+                  make_cache_map3(&tv, p.v, rows, D, p.Ps) == cudaSuccess;
+        if (!p.tma3d) {
+            if ((e = make_cache_map(&tk, p.k, rows, D, p.Ps)) != cudaSuccess) return e;
+            if ((e = make_cache_map(&tv, p.v, rows, D, p.Ps)) != cudaSuccess) return e;
+        }
     }
     p.stages = stages;
     int grid = sms * occ;

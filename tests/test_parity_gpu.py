@@ -257,3 +257,18 @@ def test_many_short_items_multi_group(groups, monkeypatch):
     check_art(w, out, bu, 1e-2, 1e-2, 1, items=items, what=f"short items, groups {groups}")
     out, _, st, _ = run_gpu(w, "dense", dev=dev)
     check_dense(w, out, items=items, what=f"short items dense, groups {groups}")
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_two_d_copies(small, k, monkeypatch):
+    """The bf16 kernels with one 2-D copy per 128-byte column half of each page
+    (the fallback when the 3-D tensor view is not accepted; ART_TMA3D=0 forces
+    it) against the oracle."""
+    monkeypatch.setenv("ART_TMA3D", "0")
+    w = small[k]
+    out, bu, st, dev = run_gpu(w, "art", 1e-2, 1e-2, 2)
+    assert st == 0
+    check_art(w, out, bu, 1e-2, 1e-2, 2, what=f"2-D copies, config {k}")
+    out, _, st, _ = run_gpu(w, "dense", dev=dev)
+    assert st == 0
+    check_dense(w, out, what=f"2-D copies dense, config {k}")
