@@ -172,6 +172,35 @@ int art_decode_static(const void* q, const void* k_cache, const void* v_cache,
                       int32_t patience, const int32_t* probe_idx, void* out,
                       int32_t* blocks_used, const art_shape* shape, void* stream);
 
+/*
+ * Key-based block selection: writes a visit list for art_decode (ART paper
+ * sec. 4, ART composed with key-centric KV selection; the score is the pooled
+ * block estimate of the FlexPrefill summary). For every item (b, g), with
+ * T = ceil(seq_len / block_size):
+ *   score_c = mean over the G query heads of g (q_h) . mean over the tokens
+ *             t < seq_len of block c (k_t)                      (fp32)
+ *   kept    = the ceil(top_frac * T) highest scores (equal scores: the lower
+ *             block index first), block 0, and the last keep_last blocks
+ *   visit_order[b][g][:] = 0, then the other kept blocks by descending index
+ *             (most recent first), then -1 up to max_visit.
+ *   top_frac in [0, 1]; keep_last >= 0; block_size 64; head_dim 64 or 128;
+ *   T <= 8192 (max_pages_per_seq * page_size <= 524288 tokens).
+ *   shape->max_visit must hold the longest possible list,
+ *   min(T_max, ceil(top_frac * T_max) + 1 + keep_last) with
+ *   T_max = ceil(max_pages_per_seq * page_size / block_size), else
+ *   ART_ERR_INVALID_ARG. num_probe and probe indices are not used.
+ *   workspace:  device scratch of art_select_workspace_bytes(shape) bytes (a
+ *               header with the status word, then the block scores); zeroed
+ *               as needed on `stream`. A page id outside the pool or a bad
+ *               seq_len gives the item an empty list and a status bit.
+ * Asynchronous on `stream`, like art_decode.
+ */
+size_t art_select_workspace_bytes(const art_shape* shape);
+int art_select_blocks(const void* q, const void* k_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, float top_frac, int32_t keep_last,
+                      int32_t* visit_order, const art_shape* shape, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
 /* Copies the device status word out of `workspace` (a blocking copy; call it
  * after the stream has finished the call of interest). Returns ART_OK or
  * ART_ERR_INVALID_ARG / ART_ERR_LAUNCH. */

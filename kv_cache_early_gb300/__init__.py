@@ -22,7 +22,8 @@ ART_OK, ART_ERR_INVALID_ARG, ART_ERR_UNSUPPORTED, ART_ERR_WORKSPACE, ART_ERR_LAU
 STATUS_BITS = {1: "bad visit entry", 2: "duplicate visit entry", 4: "bad page id", 8: "bad seq_len",
                16: "bad probe index", 32: "wait timeout", 64: "internal check failed"}
 EXPORTS = ("art_workspace_bytes", "art_decode", "dense_decode", "art_decode_static", "art_read_device_status",
-           "art_status_string", "art_last_cuda_error", "art_set_timing_events")
+           "art_status_string", "art_last_cuda_error", "art_set_timing_events",
+           "art_select_workspace_bytes", "art_select_blocks")
 
 
 class ArtShape(ctypes.Structure):
@@ -66,6 +67,10 @@ def lib(path: str = LIB_PATH) -> ctypes.CDLL:
             L.art_decode_static.restype = ctypes.c_int
             L.art_set_timing_events.argtypes = [P, P]
             L.art_set_timing_events.restype = None
+            L.art_select_workspace_bytes.argtypes = [SP]
+            L.art_select_workspace_bytes.restype = SZ
+            L.art_select_blocks.argtypes = [P, P, P, P, F32, I32, P, SP, P, SZ, P]
+            L.art_select_blocks.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -138,6 +143,23 @@ def art_decode_static(q, k_cache, v_cache, block_table, seq_lens, visit_order, e
     rc = lib().art_decode_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
                                  _ptr(visit_order), float(eps_mag), float(eps_dir), int(patience),
                                  _ptr(probe_idx), _ptr(out), _ptr(blocks_used), ctypes.byref(shape),
+                                 _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def art_select_workspace_bytes(shape: ArtShape) -> int:
+    return int(lib().art_select_workspace_bytes(ctypes.byref(shape)))
+
+
+def art_select_blocks(q, k_cache, block_table, seq_lens, top_frac, keep_last, visit_order, shape: ArtShape,
+                      workspace, stream=None, check: bool = True) -> int:
+    """Key-based block selection writing an ART visit list (see include/art.h)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else \
+        art_select_workspace_bytes(shape)
+    rc = lib().art_select_blocks(_ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(seq_lens), float(top_frac),
+                                 int(keep_last), _ptr(visit_order), ctypes.byref(shape), _ptr(workspace), ws_bytes,
                                  _stream(stream))
     if check:
         _check(rc)

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
 // ---------------------------------------------------------------------------
 thread_local std::string g_last_cuda_error = "no error";
 
-static int cuda_fail(cudaError_t e) {
+int cuda_fail(cudaError_t e) {
     g_last_cuda_error = cudaGetErrorString(e);
     return ART_ERR_LAUNCH;
 }

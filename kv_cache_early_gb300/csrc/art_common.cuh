@@ -34,6 +34,9 @@ struct WsHeader {
     int pad[8];
 };
 
+// Host: keeps the text of a failed CUDA call for art_last_cuda_error and returns ART_ERR_LAUNCH.
+int cuda_fail(cudaError_t e);
+
 // Records the first failed internal consistency check (ART_STATUS_INTERNAL).
 __device__ __forceinline__ void record_check(WsHeader* hdr, int code, int a, int b, int c) {
     if (atomicCAS(&hdr->check_code, 0, code) == 0) {
