@@ -406,6 +406,28 @@ def run_ours(args):
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e,
                "note": "KV cache resident on the device; per-step inputs and outputs copied"}
 
+    # the key-based selection that builds this workload's lists, on the device
+    selection = None
+    sel = w.notes.get("selection")
+    if sel is not None:
+        T_max = -(-w.max_pages_per_seq * w.page_size // w.block_size)
+        mv = min(T_max, int(np.ceil(sel["top_frac"] * T_max)) + 1 + sel["last"])
+        sshape = K.make_shape(**dict(w.shape_dict(), max_visit=mv))
+        vis = torch.empty((w.batch, w.num_kv_heads, mv), dtype=torch.int32, device="cuda")
+        sws = torch.zeros(K.art_select_workspace_bytes(sshape), dtype=torch.uint8, device="cuda")
+        sel_call = lambda: K.art_select_blocks(dev.q, dev.k_cache, dev.block_table, dev.seq_lens, sel["top_frac"],
+                                               sel["last"], vis, sshape, sws, stream=stream)
+        for _ in range(3):
+            sel_call()
+        ms_s = float(time_calls(sel_call, args.steps).mean())
+        host = w.visit_order.reshape(w.num_items, -1)
+        got = vis.cpu().numpy().reshape(w.num_items, -1)
+        same = sum(int(np.array_equal(got[i][got[i] >= 0], host[i][host[i] >= 0])) for i in range(w.num_items))
+        kbytes = int(w.seq_lens.sum()) * w.num_kv_heads * w.head_dim * w.elem_bytes
+        selection = {"ms_per_call": ms_s, "k_bytes": kbytes, "gbs": kbytes / (ms_s * 1e-3) / 1e9,
+                     "frac_of_peak": kbytes / (ms_s * 1e-3) / 1e9 / peak, "lists_equal_host": f"{same}/{w.num_items}",
+                     "note": "art_select_blocks: pooled block scores over all K rows, top fraction + sink + last"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, eps, p)
@@ -420,6 +442,7 @@ def run_ours(args):
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": 2 * args.steps,
                 "dense_twin": dense,
+                "selection": selection,
                 "blocks_used": {"mean": float(bu.mean()), "listed_mean": float(n.mean()),
                                 "fraction": float(bu.sum() / max(1, n.sum()))},
                 "status": status}
