@@ -132,6 +132,22 @@ __device__ __forceinline__ void st_shared_if(bool pred, float* p, float v) {
         "r"(smem_addr(p)), "f"(v)
         : "memory");
 }
+__device__ __forceinline__ void st_shared_if(bool pred, uint32_t addr, float x, float y) {  // addr 8-byte aligned
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q st.shared.v2.f32 [%1], {%2, %3};\n\t}" ::"r"((int)pred),
+        "r"(addr), "f"(x), "f"(y)
+        : "memory");
+}
+__device__ __forceinline__ void st_shared_if(bool pred, uint32_t addr, float x) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q st.shared.f32 [%1], %2;\n\t}" ::"r"((int)pred),
+        "r"(addr), "f"(x)
+        : "memory");
+}
 __device__ __forceinline__ void st_shared_if(bool pred, float* p, float x, float y) {  // p 8-byte aligned
     asm volatile(
         "{\n\t.reg .pred q;\n\t"

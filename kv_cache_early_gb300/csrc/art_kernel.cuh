@@ -540,10 +540,15 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
             mbk = fmaxf(mbk, sw[w]);
         }
         float lb = 0.f;
+        if constexpr (RGW == 1) {
+            sw[0] = 1.f;
+            lb = plb[vb * G + hme];
+        } else {
 #pragma unroll
-        for (int w = 0; w < RGW; ++w) {
-            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a row set without valid keys adds nothing
-            lb = fmaf(sw[w], plb[(vb * RGW + w) * G + hme], lb);
+            for (int w = 0; w < RGW; ++w) {
+                sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a row set without valid keys adds nothing
+                lb = fmaf(sw[w], plb[(vb * RGW + w) * G + hme], lb);
+            }
         }
         const float Mn = fmaxf(M, mbk);
         const float a = exp2f(M - Mn);
@@ -562,7 +567,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
                 float pw = 0.f;
 #pragma unroll
                 for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
-                pb = fmaf(sw[w], pw, pb);
+                pb = RGW == 1 ? pw : fmaf(sw[w], pw, pb);
             }
             // slots past the probe (or past G) hold no data: no change
             const float d = hs[j] >= 0 ? cf * (pb - lb * X[j]) : 0.f;
@@ -1450,20 +1455,24 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
     const int gbar = 1 + gi;        // named barrier of the group
     // this lane's O^T rows are d = wg DW + 16 mt + 8 r + grp; bit 2 mt + r marks a probe
     // column, byte 2 mt + r of prk holds its rank among the probe columns
-    uint32_t pbits = 0, prk = 0;
-    static_assert(2 * MT <= 4, "probe ranks of a lane fit one word");
+    // ... and pofs[2 mt + r] the byte offset of its slot in a record's partial rows
+    uint32_t pbits = 0;
+    uint32_t pofs[2 * MT];
+#pragma unroll
+    for (int k = 0; k < 2 * MT; ++k) pofs[k] = 0;
     if (kART) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int rk = prank[wg * DW + 16 * mt + 8 * r + grp];
-                if (rk >= 0) {
+                if (rk >= 0 && u0) {
                     pbits |= 1u << (2 * mt + r);
-                    prk |= (uint32_t)rk << (8 * (2 * mt + r));
+                    pofs[2 * mt + r] = (uint32_t)(((lo_lane ? C::PST : 0) + q0 + rk * C::GP) * 4);
                 }
             }
     }
+    const uint32_t part_base = smem_addr(part);
     const int mi = lane >> 3, lr = lane & 7;
     const int keyK = wg * 16 + (mi & 1) * 8 + lr;  // K rows for the S^T A fragments
     const int chK = mi >> 1;
@@ -1611,16 +1620,14 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
             if (computed) {
                 // probe partial rows (high and low parts with the split tile); predicated
                 // stores, no divergent branches
-                float* pp = part + ((size_t)rb * C::PRW + (lo_lane ? 1 : 0)) * C::PST + q0;
+                const uint32_t rec = part_base + (uint32_t)(rb * C::PRW * C::PST * 4);
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const bool on = (pbits >> (2 * m + r)) & 1u;
-                        const int rank = (int)((prk >> (8 * (2 * m + r))) & 0xffu);
-                        float* dst = pp + rank * C::GP;
-                        if (G >= 2) st_shared_if(on && u1, dst, tN[m][2 * r], tN[m][2 * r + 1]);
-                        if (G % 2) st_shared_if(on && u0 && !u1, dst, tN[m][2 * r]);
+                        if (G >= 2) st_shared_if(on && u1, rec + pofs[2 * m + r], tN[m][2 * r], tN[m][2 * r + 1]);
+                        if (G % 2) st_shared_if(on && !u1, rec + pofs[2 * m + r], tN[m][2 * r]);
                     }
                 const bool lead = wg == 0 && grp == 0;
                 st_shared_if(lead && w0, &plb[rb * G + (w0 ? q0 : 0)], lbN[0]);
