@@ -272,3 +272,37 @@ def test_two_d_copies(small, k, monkeypatch):
     out, _, st, _ = run_gpu(w, "dense", dev=dev)
     assert st == 0
     check_dense(w, out, what=f"2-D copies dense, config {k}")
+
+
+def _random_case(seed):
+    rs = np.random.default_rng(np.random.SeedSequence([97, seed]))
+    dt = "bf16" if rs.random() < 0.75 else "f32"
+    d = int(rs.choice([64, 128]))
+    G = int(rs.choice([1, 2, 4, 7, 8]))
+    hkv = int(rs.integers(1, 4))
+    B = int(rs.integers(1, 5))
+    ps = int(rs.choice([8, 16, 32, 64, 128, 256]))
+    lens = [int(x) for x in rs.integers(0, 2500, size=B)]
+    order = rs.choice(["natural", "reverse", "random", "sink_recent", "none"])
+    eps = float(rs.choice([0.0, 1e-3, 1e-2, 5e-2]))
+    p = int(rs.integers(1, 5))
+    groups = str(int(rs.integers(1, 5)))
+    plant = bool(rs.random() < 0.5)
+    w = W.build(f"random-{seed}", seed=1000 + seed, dtype=dt, batch=B, num_q_heads=G * hkv, num_kv_heads=hkv,
+                head_dim=d, page_size=ps, block_size=64, seq_lens=lens, paged="permuted", plant=plant,
+                order=None if order == "none" else str(order))
+    return w, eps, p, groups
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_shapes(seed, monkeypatch):
+    """Seeded random shapes, page sizes, lengths (empty included), orders,
+    thresholds, patience and kernel variants against the oracle."""
+    w, eps, p, groups = _random_case(seed)
+    monkeypatch.setenv("ART_GROUPS", groups)
+    out, bu, st, dev = run_gpu(w, "art", eps, eps, p)
+    assert st == 0
+    check_art(w, out, bu, eps, eps, p, what=f"random case {seed}")
+    out, _, st, _ = run_gpu(w, "dense", dev=dev)
+    assert st == 0
+    check_dense(w, out, what=f"random case {seed} dense")
