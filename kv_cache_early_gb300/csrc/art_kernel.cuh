@@ -1,34 +1,38 @@
 // art_kernel.cuh -- the persistent, warp-specialized ART decode-attention kernel.
 //
-// One CTA runs three roles over a ring of `stages` shared-memory slots, each
-// slot holding one 64-token ART block of K rows, V rows and (for an item's
-// first block) the item's G query vectors:
+// One CTA runs three roles over a ring of shared-memory slots, each slot
+// holding one 64-token ART block of K rows, V rows and (with a consumer
+// group's first block of an item) the item's G query vectors:
 //
-//   producer warp   claims work items (sequence b, KV head g) in the order the
-//                   plan kernel wrote (longest visit list first), resolves
-//                   visit entry -> logical block -> physical pages through the
-//                   block table, and fills slots with cp.async.bulk copies that
-//                   complete on the slot's mbarrier. It stops issuing an item's
-//                   blocks once the statistics warp has stopped that item.
-//   consumer warps  (kNWC) each own 8 of the block's 64 rows. Scores
-//                   s = q.k * log2(e)/sqrt(d) in fp32; the block's largest
-//                   score per head is shared through a named barrier; weights
-//                   p = 2^(s - m_blk); the block's P.V partial; and an online-
-//                   softmax fold into the running accumulators (ART paper
-//                   sec. 3.1: FlashAttention's streaming softmax, O^(t) after
-//                   t blocks). Arithmetic on packed fp32 pairs (f32x2).
-//   statistics warp merges the consumer warps' block sums and P.V at the probe
-//                   columns, in visit order, into the probe x^(i) of O^(i), and
-//                   evaluates the stability test (magnitude and direction
-//                   change both below their thresholds for `patience`
-//                   consecutive blocks, never before block 0 has been
-//                   processed) -- ART paper sec. 3.2, gist.science explainer
-//                   sec. 2.2-2.4.
+//   producer warp    claims work items (sequence b, KV head g) in the order the
+//                    plan kernel wrote (longest visit list first), resolves
+//                    visit entry -> logical block -> physical pages through the
+//                    block table, and fills slots with TMA copies (bf16: one
+//                    3-D tensor copy per page; fp32: one bulk copy per page)
+//                    that complete on the slot's mbarrier. It stops issuing an
+//                    item's blocks once the statistics warp has stopped it.
+//   consumer warps   softmax attention of the block for the item's G query
+//                    heads and the online-softmax fold into running
+//                    accumulators (ART paper sec. 3.1: FlashAttention's
+//                    streaming softmax, O^(t) after t blocks). Three forms:
+//                    - fp32: 8 warps on CUDA cores (packed f32x2 FMA), each
+//                      owning 8 of the block's rows;
+//                    - bf16, one or two groups of 4 warps (keys split, below);
+//                    - bf16, three or four groups of 4 warps (dims split).
+//                    Several groups of one CTA take alternate blocks of the
+//                    same item and merge their accumulators at its end.
+//   statistics warp  (ART only) forms, in visit order, the probe x^(i) of O^(i)
+//                    from the blocks' partials and evaluates the stability
+//                    test (magnitude and direction change both below their
+//                    thresholds for `patience` consecutive blocks, never
+//                    before block 0 has been processed) -- ART paper sec. 3.2,
+//                    gist.science explainer sec. 2.2-2.4.
 //
-// The consumers do not wait for the decision on block i before computing
-// block i+1 (G <= 4): block i+1 is held apart and folded only once block i's
-// decision says "continue"; after a stop it is discarded. For G > 4 (register
-// budget) each block waits for its own decision.
+// A consumer group folds block i into its accumulators only when block i's
+// decision has arrived, one block later (the fp32 warps with G > 4, short of
+// registers, wait for each block's own decision); a block computed past a stop
+// is discarded. Where no stop is possible at a block, the statistics warp sends
+// "continue" before computing the block's statistics.
 //
 // The statistics avoid cancellation: the change of the probe over block i is
 // formed directly, delta = b (P.V_probe - l_blk x^(i-1)) / L_i, the norm
