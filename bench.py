@@ -427,6 +427,19 @@ def run_ours(args):
         selection = {"ms_per_call": ms_s, "k_bytes": kbytes, "gbs": kbytes / (ms_s * 1e-3) / 1e9,
                      "frac_of_peak": kbytes / (ms_s * 1e-3) / 1e9 / peak, "lists_equal_host": f"{same}/{w.num_items}",
                      "note": "art_select_blocks: pooled block scores over all K rows, top fraction + sink + last"}
+        # the same kept blocks in importance order (highest score first): the blocks ART reads
+        K.art_select_blocks(dev.q, dev.k_cache, dev.block_table, dev.seq_lens, sel["top_frac"], sel["last"], vis,
+                            sshape, sws, stream=stream, order=1)
+        ishape = K.make_shape(**dict(w.shape_dict(), max_visit=mv))
+        iws = torch.zeros(K.art_workspace_bytes(ishape), dtype=torch.uint8, device="cuda")
+        bu_imp = torch.empty_like(dev.blocks_used)
+        K.art_decode(dev.q, dev.k_cache, dev.v_cache, dev.block_table, dev.seq_lens, vis, eps, eps, p, dev.probe_idx,
+                     torch.empty_like(dev.out), bu_imp, ishape, iws, stream)
+        torch.cuda.synchronize()
+        bi = bu_imp.cpu().numpy().reshape(-1)
+        n = w.visit_lengths()
+        selection["blocks_used_fraction"] = {"recency_order": float(bu.sum() / max(1, n.sum())),
+                                             "importance_order": float(bi.sum() / max(1, n.sum()))}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -181,8 +181,11 @@ int art_decode_static(const void* q, const void* k_cache, const void* v_cache,
  *             t < seq_len of block c (k_t)                      (fp32)
  *   kept    = the ceil(top_frac * T) highest scores (equal scores: the lower
  *             block index first), block 0, and the last keep_last blocks
- *   visit_order[b][g][:] = 0, then the other kept blocks by descending index
- *             (most recent first), then -1 up to max_visit.
+ *   visit_order[b][g][:] = 0, then the other kept blocks, then -1 up to
+ *             max_visit; order 0: by descending index (most recent first),
+ *             order 1: by descending score (importance first; equal scores:
+ *             the lower block index first) -- the two visit orders the ART
+ *             paper sec. 4 discusses.
  *   top_frac in [0, 1]; keep_last >= 0; block_size 64; head_dim 64 or 128;
  *   T <= 8192 (max_pages_per_seq * page_size <= 524288 tokens).
  *   shape->max_visit must hold the longest possible list,
@@ -198,8 +201,8 @@ int art_decode_static(const void* q, const void* k_cache, const void* v_cache,
 size_t art_select_workspace_bytes(const art_shape* shape);
 int art_select_blocks(const void* q, const void* k_cache, const int32_t* block_table,
                       const int32_t* seq_lens, float top_frac, int32_t keep_last,
-                      int32_t* visit_order, const art_shape* shape, void* workspace,
-                      size_t workspace_bytes, void* stream);
+                      int32_t order, int32_t* visit_order, const art_shape* shape,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Copies the device status word out of `workspace` (a blocking copy; call it
  * after the stream has finished the call of interest). Returns ART_OK or

@@ -69,7 +69,7 @@ def lib(path: str = LIB_PATH) -> ctypes.CDLL:
             L.art_set_timing_events.restype = None
             L.art_select_workspace_bytes.argtypes = [SP]
             L.art_select_workspace_bytes.restype = SZ
-            L.art_select_blocks.argtypes = [P, P, P, P, F32, I32, P, SP, P, SZ, P]
+            L.art_select_blocks.argtypes = [P, P, P, P, F32, I32, I32, P, SP, P, SZ, P]
             L.art_select_blocks.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -154,12 +154,14 @@ def art_select_workspace_bytes(shape: ArtShape) -> int:
 
 
 def art_select_blocks(q, k_cache, block_table, seq_lens, top_frac, keep_last, visit_order, shape: ArtShape,
-                      workspace, stream=None, check: bool = True) -> int:
-    """Key-based block selection writing an ART visit list (see include/art.h)."""
+                      workspace, stream=None, check: bool = True, order: int = 0) -> int:
+    """Key-based block selection writing an ART visit list (see include/art.h);
+    order 0: most recent first, 1: highest score first."""
     ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else \
         art_select_workspace_bytes(shape)
     rc = lib().art_select_blocks(_ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(seq_lens), float(top_frac),
-                                 int(keep_last), _ptr(visit_order), ctypes.byref(shape), _ptr(workspace), ws_bytes,
+                                 int(keep_last), int(order), _ptr(visit_order), ctypes.byref(shape),
+                                 _ptr(workspace), ws_bytes,
                                  _stream(stream))
     if check:
         _check(rc)

@@ -9,7 +9,8 @@
 // over the tokens of the block below seq_len. Kept: the ceil(top_frac * T)
 // highest scores (equal scores: the lower block index first), block 0 (the
 // attention sink) and the last keep_last blocks. Written order: block 0, then
-// the other kept blocks by descending index (most recent first), then -1.
+// the other kept blocks by descending index (most recent first) or, on request,
+// by descending score (importance first), then -1.
 //
 // Two kernels: art_score_kernel (many CTAs per item, each scoring a run of
 // blocks; bound by reading K once) and art_topk_kernel (one CTA per item: a
@@ -34,6 +35,7 @@ struct SelectParams {
     int32_t* visit;  // [num_items][max_visit]
     WsHeader* hdr;
     int B, Hq, Hkv, Ps, max_pages, max_visit, num_pages, maxT, keep_last;
+    int by_score;  // list order: 0 descending index, 1 descending score
     float top_frac;
 };
 
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kScoreThreads) art_score_kernel(const SelectPa
     constexpr int CPR = D * ELT / 16;  // 16-byte chunks of a row
     constexpr int RPS = 32 / CPR;      // rows per warp step
     constexpr int EPC = 16 / ELT;      // elements per chunk
-    constexpr int UNR = 4;             // row steps in flight per lane
+    constexpr int UNR = 8;             // row steps in flight per lane
     __shared__ float qbar[D];
     const int item = blockIdx.y;
     const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
@@ -78,28 +80,29 @@ __global__ void __launch_bounds__(kScoreThreads) art_score_kernel(const SelectPa
     for (int e = 0; e < EPC; ++e) qv[e] = qbar[ch * EPC + e];
     const int32_t* trow = p.block_table + (size_t)b * p.max_pages;
     const char* kb = static_cast<const char*>(p.k);
+    const int PR = p.Ps < kBK ? p.Ps : kBK;  // rows of the block in one page
     for (int c = c0 + warp; c < min(c0 + kScoreBlocksPerCta, T); c += kScoreThreads / 32) {
         const int t0 = c * kBK, nv = min(kBK, seq_len - t0);
+        // the block's pages (at most 8), one per lane, then shared by shuffles
+        const int npg = (nv + PR - 1) / PR;
+        int mypg = 0;
+        if (lane < npg) mypg = __ldg(&trow[(t0 + lane * PR) / p.Ps]);
+        const bool badpg = lane < npg && (mypg < 0 || mypg >= p.num_pages);
+        bool bad = __any_sync(0xffffffffu, badpg);
+        const int r_in = (t0 % p.Ps);  // first row of the block inside its page (pages longer than a block)
         float acc = 0.f;
-        bool bad = false;
-        for (int r0 = 0; r0 < nv; r0 += RPS * UNR) {
+        for (int r0 = 0; r0 < nv && !bad; r0 += RPS * UNR) {
             uint4 v[UNR];
             bool on[UNR];
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
                 const int r = r0 + u * RPS + rsub;
                 on[u] = r < nv;
+                const int pg = __shfl_sync(0xffffffffu, mypg, on[u] ? r / PR : 0);
                 v[u] = make_uint4(0u, 0u, 0u, 0u);
                 if (on[u]) {
-                    const int t = t0 + r;
-                    const int pg = __ldg(&trow[t / p.Ps]);
-                    if (pg < 0 || pg >= p.num_pages) {
-                        bad = true;
-                        on[u] = false;
-                    } else {
-                        const size_t row = ((size_t)pg * p.Hkv + g) * p.Ps + (t % p.Ps);
-                        v[u] = __ldg(reinterpret_cast<const uint4*>(kb + row * (D * ELT)) + ch);
-                    }
+                    const size_t row = ((size_t)pg * p.Hkv + g) * p.Ps + r_in + (r % PR);
+                    v[u] = __ldg(reinterpret_cast<const uint4*>(kb + row * (D * ELT)) + ch);
                 }
             }
 #pragma unroll
@@ -120,7 +123,6 @@ __global__ void __launch_bounds__(kScoreThreads) art_score_kernel(const SelectPa
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
             if (bad) atomicOr(&p.hdr->status, ART_STATUS_BAD_PAGE);
             p.scores[(size_t)item * p.maxT + c] = bad ? __int_as_float(0x7fc00000) : acc / (float)nv;
@@ -194,15 +196,16 @@ __global__ void __launch_bounds__(kTopkThreads) art_topk_kernel(const SelectPara
     for (int c = tid; c < T; c += kTopkThreads)
         if (c == 0 || c >= T - p.keep_last) kept[c] = 1;
     __syncthreads();
-    // output positions: block 0 first, then kept blocks by descending index, by a
-    // block-wide exclusive scan over j = T - 1 - c (c = T-1 .. 1)
+    // output positions: block 0 first, then the other kept blocks in the requested
+    // order, by a block-wide exclusive scan over the candidates j: block T - 1 - j
+    // (descending index) or the block of rank j (descending score)
     constexpr int PER = kMaxSelectBlocks / kTopkThreads;
+    auto cand = [&](int j) -> int { return p.by_score ? (j < T ? idx[j] : 0) : T - 1 - j; };
     int f[PER], run = 0;
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-        const int j = tid * PER + k;
-        const int c = T - 1 - j;
-        f[k] = (c >= 1 && kept[c]) ? 1 : 0;
+        const int c = cand(tid * PER + k);
+        f[k] = (c >= 1 && c < T && kept[c]) ? 1 : 0;
         run += f[k];
     }
     const int lane = tid & 31, wid = tid >> 5;
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(kTopkThreads) art_topk_kernel(const SelectPara
     const int total = 1 + s_wsum[kTopkThreads / 32 - 1];
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-        const int c = T - 1 - (tid * PER + k);
+        const int c = cand(tid * PER + k);
         if (f[k]) {
             if (pos < p.max_visit) out[pos] = c;
             ++pos;
@@ -256,8 +259,8 @@ size_t art_select_workspace_bytes(const art_shape* shape) {
 }
 
 int art_select_blocks(const void* q, const void* k_cache, const int32_t* block_table, const int32_t* seq_lens,
-                      float top_frac, int32_t keep_last, int32_t* visit_order, const art_shape* shape, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+                      float top_frac, int32_t keep_last, int32_t order, int32_t* visit_order, const art_shape* shape,
+                      void* workspace, size_t workspace_bytes, void* stream) {
     if (!shape || !q || !k_cache || !block_table || !seq_lens || !visit_order || !workspace) return ART_ERR_INVALID_ARG;
     const art_shape& s = *shape;
     if (s.batch < 1 || s.num_q_heads < 1 || s.num_kv_heads < 1 || s.num_q_heads % s.num_kv_heads != 0 ||
@@ -266,7 +269,8 @@ int art_select_blocks(const void* q, const void* k_cache, const int32_t* block_t
     if (s.dtype != ART_DTYPE_BF16 && s.dtype != ART_DTYPE_F32) return ART_ERR_INVALID_ARG;
     if (s.head_dim != 64 && s.head_dim != 128) return ART_ERR_UNSUPPORTED;
     if (s.block_size != kBK) return ART_ERR_UNSUPPORTED;
-    if (!(top_frac >= 0.f && top_frac <= 1.f) || keep_last < 0) return ART_ERR_INVALID_ARG;
+    if (!(top_frac >= 0.f && top_frac <= 1.f) || keep_last < 0 || (order != 0 && order != 1))
+        return ART_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(k_cache) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return ART_ERR_INVALID_ARG;
     const long long maxT = ((long long)s.max_pages_per_seq * s.page_size + kBK - 1) / kBK;
@@ -298,6 +302,7 @@ int art_select_blocks(const void* q, const void* k_cache, const int32_t* block_t
     p.num_pages = s.num_pages_total;
     p.maxT = (int)maxT;
     p.keep_last = keep_last;
+    p.by_score = order;
     p.top_frac = top_frac;
     const int items = s.batch * s.num_kv_heads;
     const dim3 grid((unsigned)((maxT + kScoreBlocksPerCta - 1) / kScoreBlocksPerCta), (unsigned)items);

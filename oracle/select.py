@@ -14,7 +14,8 @@ sec. 4), in fp64 on the exact bf16 / fp32 input values, for every item
     score_c = qbar . kbar_c
     kept    = the ceil(top_frac * T) highest scores (equal scores: lower
               block index first), block 0, the last keep_last blocks
-    list    = [0] + the other kept blocks in descending index order
+    list    = [0] + the other kept blocks in descending index order (recency),
+              or by descending score, equal scores lower index first (importance)
 
 Each step is written out with plain loops over blocks and rows.
 """
@@ -52,7 +53,7 @@ def block_scores(q, k_cache, block_table, seq_len, b, g, *, num_q_heads, num_kv_
     return scores
 
 
-def kept_list(scores, top_frac: float, keep_last: int):
+def kept_list(scores, top_frac: float, keep_last: int, order: str = "recency"):
     """The visit list from one item's scores."""
     T = len(scores)
     if T == 0:
@@ -60,10 +61,12 @@ def kept_list(scores, top_frac: float, keep_last: int):
     k = min(T, math.ceil(top_frac * T))
     ranked = sorted(range(T), key=lambda c: (-scores[c], c))
     kept = set(ranked[:k]) | {0} | set(range(max(0, T - keep_last), T))
+    if order == "importance":
+        return [0] + [c for c in ranked if c in kept and c != 0]
     return [0] + sorted((c for c in kept if c != 0), reverse=True)
 
 
-def select_blocks(w, top_frac: float, keep_last: int, items=None):
+def select_blocks(w, top_frac: float, keep_last: int, items=None, order: str = "recency"):
     """Lists and scores for a workloads.Workload (all items, or `items`)."""
     items = range(w.num_items) if items is None else items
     out = {}
@@ -72,5 +75,5 @@ def select_blocks(w, top_frac: float, keep_last: int, items=None):
         sc = block_scores(w.q, w.k_cache, w.block_table, w.seq_lens[b], b, g, num_q_heads=w.num_q_heads,
                           num_kv_heads=w.num_kv_heads, page_size=w.page_size, block_size=w.block_size,
                           dtype=w.dtype)
-        out[int(it)] = (kept_list(sc, top_frac, keep_last), sc)
+        out[int(it)] = (kept_list(sc, top_frac, keep_last, order), sc)
     return out

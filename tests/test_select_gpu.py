@@ -20,7 +20,7 @@ import kv_cache_early_gb300 as K  # noqa: E402
 TIE_REL = 1e-5
 
 
-def run_select(w, top_frac, keep_last, max_visit=None):
+def run_select(w, top_frac, keep_last, max_visit=None, order=0):
     dev = K.DeviceInputs(w)
     T_max = -(-w.max_pages_per_seq * w.page_size // w.block_size)
     need = min(T_max, int(np.ceil(top_frac * T_max)) + 1 + keep_last)
@@ -28,7 +28,8 @@ def run_select(w, top_frac, keep_last, max_visit=None):
     shape = K.make_shape(**dict(w.shape_dict(), max_visit=mv))
     vis = torch.full((w.batch, w.num_kv_heads, mv), -7, dtype=torch.int32, device="cuda")
     ws = torch.zeros(K.art_select_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
-    K.art_select_blocks(dev.q, dev.k_cache, dev.block_table, dev.seq_lens, top_frac, keep_last, vis, shape, ws)
+    K.art_select_blocks(dev.q, dev.k_cache, dev.block_table, dev.seq_lens, top_frac, keep_last, vis, shape, ws,
+                        order=order)
     torch.cuda.synchronize()
     return vis.cpu().numpy().reshape(w.num_items, mv), K.art_read_device_status(ws)
 
@@ -115,3 +116,25 @@ def test_select_then_decode_matches_host_lists():
     torch.cuda.synchronize()
     assert np.array_equal(dev.blocks_used.cpu().numpy(), a_bu)
     assert np.array_equal(dev.out.float().cpu().numpy(), a_out)
+
+
+@pytest.mark.parametrize("k", [2, 4, 5])
+def test_select_importance_order(k):
+    """Order 1: block 0, then the kept blocks by descending score. Same kept set
+    as order 0 (up to ties at the cut); the sequence must descend in the
+    oracle's scores up to the tie tolerance."""
+    w = W.config(k, small=True)
+    got0, st0 = run_select(w, 0.25, 8)
+    got1, st1 = run_select(w, 0.25, 8, order=1)
+    assert st0 == 0 and st1 == 0
+    ref = S.select_blocks(w, 0.25, 8, order="importance")
+    for it, (lst, sc) in ref.items():
+        d0 = [int(x) for x in got0[it] if x >= 0]
+        d1 = [int(x) for x in got1[it] if x >= 0]
+        assert sorted(d0) == sorted(d1), f"item {it}: kept sets differ between orders"
+        if d1 == lst:
+            continue
+        assert d1[0] == 0
+        scale = max(float(np.abs(sc).mean()), 1e-30)
+        for a, b in zip(d1[1:], d1[2:]):
+            assert sc[a] >= sc[b] - TIE_REL * scale, f"item {it}: {a} before {b}"

@@ -65,3 +65,16 @@ def test_hand_scores_on_a_tiny_paged_cache():
 ])
 def test_list_rules(scores, frac, last, expect):
     assert S.kept_list(np.asarray(scores, np.float64), frac, last) == expect
+
+
+@pytest.mark.parametrize("scores,frac,last,expect", [
+    ([5, 1, 9, 9, 2, 7], 0.5, 0, [0, 2, 3, 5]),      # by score 9, 9 (lower index first), 7
+    ([0, 3, 2, 1, 4], 0.0, 2, [0, 4, 3]),            # block 0 and the last two, by score 4 > 1
+    ([0, 3, 2, 1, 4], 1.0, 0, [0, 4, 1, 2, 3]),      # everything by score
+    ([7, 1, 1, 5], 0.25, 1, [0, 3]),                 # top block is 0 itself; last block 3
+])
+def test_importance_order(scores, frac, last, expect):
+    assert S.kept_list(np.asarray(scores, np.float64), frac, last, order="importance") == expect
+    # the same kept set as the recency order
+    rec = S.kept_list(np.asarray(scores, np.float64), frac, last)
+    assert sorted(rec) == sorted(expect)
