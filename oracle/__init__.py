@@ -57,13 +57,14 @@ class Oracle:
         lib.oracle_art.argtypes = [ctypes.POINTER(_Shape), P, P, P, P, P, P,
                                    ctypes.c_double, ctypes.c_double, ctypes.c_int32, P,
                                    ctypes.c_int32, P, ctypes.c_int32, P,
-                                   P, P, P, P, P, ctypes.c_int32]
+                                   P, P, P, P, P, ctypes.c_int32, ctypes.c_int32]
         lib.oracle_art.restype = ctypes.c_int
         self.lib = lib
 
     def run(self, shape: dict, q, k_cache, v_cache, block_table, seq_lens, visit_order, *,
             eps_mag: float = 0.0, eps_dir: float = 0.0, patience: int = 1, probe_idx=None,
-            mode: str = "art", items=None, forced=None, trace: bool = False, threads: int = 0) -> dict:
+            mode: str = "art", items=None, forced=None, trace: bool = False, threads: int = 0,
+            probe_heads: int = 0) -> dict:
         """Run the oracle.
 
         shape: dict with the fields of the layout (batch, num_q_heads, num_kv_heads,
@@ -74,6 +75,8 @@ class Oracle:
         items: optional list of item ids b * num_kv_heads + g (default: all).
         eps values are compared in fp64 exactly as given (pass the float32 value
         used on the device to reproduce its thresholds).
+        probe_heads: the probe is formed by query heads 0 .. probe_heads-1 of each
+        group (0: all G heads).
         Returns dict(out [n_items, G, d] fp64, blocks_used, status, trace_mag,
         trace_dir (None unless trace), threads).
         """
@@ -109,7 +112,8 @@ class Oracle:
                                  _ptr(block_table), _ptr(seq_lens), _ptr(visit_order),
                                  float(eps_mag), float(eps_dir), int(patience), _ptr(probe), m,
                                  _ptr(its), n_items if its is not None else 0, _ptr(fz),
-                                 _ptr(out), _ptr(bu), _ptr(st), _ptr(tm), _ptr(td), int(threads))
+                                 _ptr(out), _ptr(bu), _ptr(st), _ptr(tm), _ptr(td), int(threads),
+                                 int(probe_heads))
         if nt < 0:
             raise ValueError(f"oracle rejected its arguments (code {nt})")
         return dict(out=out, blocks_used=bu, status=st, trace_mag=tm, trace_dir=td, threads=nt)
@@ -129,7 +133,8 @@ def run(*args, **kw) -> dict:
 
 
 def run_workload(w, *, mode: str = "art", items=None, forced=None, trace: bool = False, threads: int = 0,
-                 eps_mag=None, eps_dir=None, patience=None, visit_order="default", orc=None) -> dict:
+                 eps_mag=None, eps_dir=None, patience=None, visit_order="default", orc=None,
+                 probe_heads: int = 0) -> dict:
     """Convenience wrapper taking a workload object with the usual attributes.
     Thresholds default to the workload's, rounded to float32 as the device sees them.
     `orc` selects another build of the oracle (default: the stock one)."""
@@ -142,4 +147,4 @@ def run_workload(w, *, mode: str = "art", items=None, forced=None, trace: bool =
     return (orc or default()).run(sh, w.q, w.k_cache, w.v_cache, w.block_table, w.seq_lens, vo,
         eps_mag=float(np.float32(em)), eps_dir=float(np.float32(ed)),
         patience=w.patience if patience is None else patience, probe_idx=w.probe_idx,
-        mode=mode, items=items, forced=forced, trace=trace, threads=threads)
+        mode=mode, items=items, forced=forced, trace=trace, threads=threads, probe_heads=probe_heads)

@@ -17,6 +17,8 @@
  *   gist.science "2.2 Stabilitaetsbasiertes Terminierungskriterium",
  *   "2.3 Geduld-Mechanismus", "2.4 Integration und Korrektheit"):
  *     x^(i)    = concat over the G query heads of the group of O^(i)_h[probe]
+ *                (or over the first probe_heads of them: the paper's probe is
+ *                a fragment of one head's output, sec. 3.2)
  *     n_i      = ||x^(i)||_2
  *     d_mag_i  = | n_i - n_{i-1} | / n_{i-1}                      (i >= 2)
  *     d_dir_i  = max(0, 1 - <x^(i), x^(i-1)> / (n_i n_{i-1}))     (i >= 2)
@@ -70,6 +72,7 @@ typedef struct {
     const int32_t *block_table, *seq_lens, *visit_order, *probe_idx;
     double eps_mag, eps_dir;
     int32_t patience;
+    int32_t probe_heads; /* heads 0 .. probe_heads-1 of the group form the probe */
     int32_t mode; /* 0 = dense (all listed blocks), 1 = ART rule, 2 = forced */
     const int32_t *items;
     const int32_t *forced;
@@ -211,8 +214,9 @@ static void run_item(job_t *J, int slot)
                 }
             }
             if (L[i - 1] == 0) seen0 = 1;
+            const int PH = J->probe_heads;
             double nn = 0.0;
-            for (int h = 0; h < G; ++h)
+            for (int h = 0; h < PH; ++h)
                 for (int k = 0; k < m; ++k) {
                     x[h * m + k] = Nm[h * m + k] / Z[h];
                     nn += x[h * m + k] * x[h * m + k];
@@ -221,7 +225,7 @@ static void run_item(job_t *J, int slot)
             int stable = 0;
             if (i >= 2) {
                 double dot = 0.0;
-                for (int k = 0; k < G * m; ++k) dot += x[k] * xp[k];
+                for (int k = 0; k < PH * m; ++k) dot += x[k] * xp[k];
                 double dmag = fabs(nn - nprev) / nprev;
                 double ddir = 1.0 - dot / (nn * nprev);
                 if (ddir < 0.0) ddir = 0.0;
@@ -277,15 +281,16 @@ static void *worker(void *arg)
  * Outputs per item slot k: out[k][G][d], blocks_used[k], item_status[k],
  * and (if non-NULL) trace_mag[k][max_visit], trace_dir[k][max_visit]
  * holding d_mag_i / d_dir_i at index i-1 (NaN where undefined or not reached).
- * num_threads <= 0 uses every online core. Returns the thread count used,
- * or a negative value on a bad argument.
+ * num_threads <= 0 uses every online core. probe_heads (1..G, or 0 for all G)
+ * selects the query heads whose outputs form the probe. Returns the thread
+ * count used, or a negative value on a bad argument.
  */
 int oracle_art(const oracle_shape *sh, const void *q, const void *k_cache, const void *v_cache,
                const int32_t *block_table, const int32_t *seq_lens, const int32_t *visit_order,
                double eps_mag, double eps_dir, int32_t patience, const int32_t *probe_idx,
                int32_t mode, const int32_t *items, int32_t num_items, const int32_t *forced,
                double *out, int32_t *blocks_used, int32_t *item_status,
-               double *trace_mag, double *trace_dir, int32_t num_threads)
+               double *trace_mag, double *trace_dir, int32_t num_threads, int32_t probe_heads)
 {
     if (!sh || !q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !blocks_used ||
         !item_status)
@@ -295,6 +300,7 @@ int oracle_art(const oracle_shape *sh, const void *q, const void *k_cache, const
     if (mode == 1 && (patience < 1 || !probe_idx || sh->num_probe <= 0)) return -4;
     if (mode == 2 && !forced) return -5;
     if (sh->dtype != 0 && sh->dtype != 1) return -6;
+    if (probe_heads < 0 || probe_heads > sh->num_q_heads / sh->num_kv_heads) return -7;
     if (!items) num_items = sh->batch * sh->num_kv_heads;
 
     job_t J;
@@ -302,6 +308,7 @@ int oracle_art(const oracle_shape *sh, const void *q, const void *k_cache, const
     J.sh = sh; J.q = q; J.k = k_cache; J.v = v_cache;
     J.block_table = block_table; J.seq_lens = seq_lens; J.visit_order = visit_order;
     J.probe_idx = probe_idx; J.eps_mag = eps_mag; J.eps_dir = eps_dir; J.patience = patience;
+    J.probe_heads = probe_heads > 0 ? probe_heads : sh->num_q_heads / sh->num_kv_heads;
     J.mode = mode; J.items = items; J.forced = forced; J.num_items = num_items;
     J.out = out; J.blocks_used = blocks_used; J.item_status = item_status;
     J.trace_mag = trace_mag; J.trace_dir = trace_dir;
