@@ -134,6 +134,24 @@ int art_decode(const void* q, const void* k_cache, const void* v_cache,
                int32_t* blocks_used, const art_shape* shape, void* workspace,
                size_t workspace_bytes, void* stream);
 
+/* Options of art_decode_ex (an addition of this library for ablations). */
+typedef struct art_options {
+    int32_t probe_heads; /* 0: the probe concatenates all G query heads of the
+                            group (art_decode); 1..G: only heads 0..probe_heads-1
+                            (probe_heads = 1 is closest to the ART paper's probe,
+                            a fragment of one head's output, sec. 3.2) */
+    int32_t reserved[7]; /* must be zero */
+} art_options;
+
+/* art_decode with options (NULL: the defaults, i.e. art_decode). A
+ * probe_heads outside 0..G or a non-zero reserved field: ART_ERR_INVALID_ARG. */
+int art_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_table, const int32_t* seq_lens,
+                  const int32_t* visit_order, float eps_mag, float eps_dir,
+                  int32_t patience, const int32_t* probe_idx, void* out,
+                  int32_t* blocks_used, const art_shape* shape, void* workspace,
+                  size_t workspace_bytes, void* stream, const art_options* options);
+
 /*
  * The full-scan twin: the same blocked attention over every listed block,
  * with no probe, no test and no termination. probe_idx and num_probe are not

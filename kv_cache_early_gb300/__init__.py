@@ -21,7 +21,7 @@ ART_DTYPE_BF16, ART_DTYPE_F32 = 0, 1
 ART_OK, ART_ERR_INVALID_ARG, ART_ERR_UNSUPPORTED, ART_ERR_WORKSPACE, ART_ERR_LAUNCH = 0, -1, -2, -3, -4
 STATUS_BITS = {1: "bad visit entry", 2: "duplicate visit entry", 4: "bad page id", 8: "bad seq_len",
                16: "bad probe index", 32: "wait timeout", 64: "internal check failed"}
-EXPORTS = ("art_workspace_bytes", "art_decode", "dense_decode", "art_decode_static", "art_read_device_status",
+EXPORTS = ("art_workspace_bytes", "art_decode", "art_decode_ex", "dense_decode", "art_decode_static", "art_read_device_status",
            "art_status_string", "art_last_cuda_error", "art_set_timing_events",
            "art_select_workspace_bytes", "art_select_blocks")
 
@@ -30,6 +30,10 @@ class ArtShape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "block_size",
         "max_pages_per_seq", "max_visit", "num_probe", "num_pages_total", "dtype")]
+
+
+class ArtOptions(ctypes.Structure):
+    _fields_ = [("probe_heads", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
 
 
 class ArtError(RuntimeError):
@@ -63,6 +67,9 @@ def lib(path: str = LIB_PATH) -> ctypes.CDLL:
             L.art_status_string.restype = ctypes.c_char_p
             L.art_last_cuda_error.argtypes = []
             L.art_last_cuda_error.restype = ctypes.c_char_p
+            L.art_decode_ex.argtypes = [P, P, P, P, P, P, F32, F32, I32, P, P, P, SP, P, SZ, P,
+                                        ctypes.POINTER(ArtOptions)]
+            L.art_decode_ex.restype = ctypes.c_int
             L.art_decode_static.argtypes = [P, P, P, P, P, P, F32, F32, I32, P, P, P, SP, P]
             L.art_decode_static.restype = ctypes.c_int
             L.art_set_timing_events.argtypes = [P, P]
@@ -132,6 +139,23 @@ def dense_decode(q, k_cache, v_cache, block_table, seq_lens, visit_order, out, s
     rc = lib().dense_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
                             _ptr(visit_order), _ptr(out), ctypes.byref(shape), _ptr(workspace), ws_bytes,
                             _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def art_decode_ex(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience,
+                  probe_idx, out, blocks_used, shape: ArtShape, workspace, stream=None, check: bool = True,
+                  probe_heads: int = 0) -> int:
+    """art_decode with options: probe_heads 1..G forms the probe from query heads
+    0 .. probe_heads-1 of each group (0: all G)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else \
+        art_workspace_bytes(shape)
+    opts = ArtOptions(probe_heads=int(probe_heads))
+    rc = lib().art_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+                             _ptr(visit_order), float(eps_mag), float(eps_dir), int(patience), _ptr(probe_idx),
+                             _ptr(out), _ptr(blocks_used), ctypes.byref(shape), _ptr(workspace), ws_bytes,
+                             _stream(stream), ctypes.byref(opts))
     if check:
         _check(rc)
     return rc
@@ -223,11 +247,16 @@ class DeviceInputs:
         nbytes = art_workspace_bytes(self.shape)
         self.workspace = torch.zeros((nbytes + 15) // 16 * 16, dtype=torch.uint8, device=device)
 
-    def art(self, eps_mag, eps_dir, patience, stream=None, visit_order="default", out=None, blocks_used=None):
+    def art(self, eps_mag, eps_dir, patience, stream=None, visit_order="default", out=None, blocks_used=None,
+            probe_heads: int = 0):
         vo = self.visit_order if isinstance(visit_order, str) else visit_order
-        art_decode(self.q, self.k_cache, self.v_cache, self.block_table, self.seq_lens, vo, eps_mag, eps_dir,
-                   patience, self.probe_idx, self.out if out is None else out,
-                   self.blocks_used if blocks_used is None else blocks_used, self.shape, self.workspace, stream)
+        args = (self.q, self.k_cache, self.v_cache, self.block_table, self.seq_lens, vo, eps_mag, eps_dir,
+                patience, self.probe_idx, self.out if out is None else out,
+                self.blocks_used if blocks_used is None else blocks_used, self.shape, self.workspace, stream)
+        if probe_heads:
+            art_decode_ex(*args, probe_heads=probe_heads)
+        else:
+            art_decode(*args)
 
     def dense(self, stream=None, visit_order="default", out=None):
         vo = self.visit_order if isinstance(visit_order, str) else visit_order

@@ -202,10 +202,11 @@ template <bool kART>
 static int run(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                const int32_t* seq_lens, const int32_t* visit_order, float eps_mag, float eps_dir, int32_t patience,
                const int32_t* probe_idx, void* out, int32_t* blocks_used, const art_shape* shape, void* workspace,
-               size_t workspace_bytes, void* stream, LaunchInfo* li) {
+               size_t workspace_bytes, void* stream, LaunchInfo* li, int probe_heads = 0) {
     const int rc = check_shape(shape);
     if (rc != ART_OK) return rc;
     const art_shape& s = *shape;
+    if (probe_heads < 0 || probe_heads > s.num_q_heads / s.num_kv_heads) return ART_ERR_INVALID_ARG;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace) return ART_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
         return ART_ERR_INVALID_ARG;
@@ -270,6 +271,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     p.eps_mag = eps_mag;
     p.eps_dir = eps_dir;
     p.patience = patience;
+    p.ph = probe_heads > 0 ? probe_heads : s.num_q_heads / s.num_kv_heads;
     p.tma3d = 0;
     if (t_events.start && (e = cudaEventRecord(t_events.start, st)) != cudaSuccess) return cuda_fail(e);
     e = dispatch<kART>(s, p, st, env_stages(), li);
@@ -295,6 +297,19 @@ int art_decode(const void* q, const void* k_cache, const void* v_cache, const in
                size_t workspace_bytes, void* stream) {
     return run<true>(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience, probe_idx,
                      out, blocks_used, shape, workspace, workspace_bytes, stream, nullptr);
+}
+
+int art_decode_ex(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                  const int32_t* seq_lens, const int32_t* visit_order, float eps_mag, float eps_dir, int32_t patience,
+                  const int32_t* probe_idx, void* out, int32_t* blocks_used, const art_shape* shape, void* workspace,
+                  size_t workspace_bytes, void* stream, const art_options* options) {
+    if (options) {
+        for (int i = 0; i < 7; ++i)
+            if (options->reserved[i] != 0) return ART_ERR_INVALID_ARG;
+    }
+    return run<true>(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience, probe_idx,
+                     out, blocks_used, shape, workspace, workspace_bytes, stream, nullptr,
+                     options ? options->probe_heads : 0);
 }
 
 int dense_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,

@@ -71,6 +71,7 @@ struct Params {
     int tma3d;  // tensor-core path: one 3-D copy per page (else one 2-D copy per 128-byte column half)
     float eps_mag, eps_dir;
     int patience;
+    int ph;  // query heads 0 .. ph-1 of a group form the probe
 };
 
 // Launch geometry chosen for one call.

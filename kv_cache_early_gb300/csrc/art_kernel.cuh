@@ -469,12 +469,13 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
     const int lane = threadIdx.x & 31;
     const int m = p.m;
     // probe slot k = lane + 32 j is word k of a partial row: head k % GP, rank k / GP
-    // (the statistics do not depend on the order of the probe coordinates)
+    // (the statistics do not depend on the order of the probe coordinates); heads
+    // from p.ph on are not part of the probe
     int hs[SPL];
 #pragma unroll
     for (int j = 0; j < SPL; ++j) {
         const int k = lane + 32 * j;
-        hs[j] = (k % C::GP < G && k / C::GP < m) ? k % C::GP : -1;
+        hs[j] = (k % C::GP < p.ph && k / C::GP < m) ? k % C::GP : -1;
     }
     // every slot of this lane belongs to head lane % GP, whose running max and
     // weight sum the lane keeps

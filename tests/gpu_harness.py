@@ -71,12 +71,13 @@ def is_tie(trace_mag, trace_dir, lo, hi, eps_mag, eps_dir):
     return False
 
 
-def check_art(w, gpu_out, gpu_bu, eps_mag, eps_dir, patience, items=None, visit_order="default", what=""):
+def check_art(w, gpu_out, gpu_bu, eps_mag, eps_dir, patience, items=None, visit_order="default", what="",
+              probe_heads=0):
     """blocks_used (exact up to ties) and outputs against the oracle.
     Returns dict(ties, mismatches, items, mean_bu)."""
     its = np.arange(w.num_items) if items is None else np.asarray(items)
     r = O.run_workload(w, items=None if items is None else its, eps_mag=eps_mag, eps_dir=eps_dir,
-                       patience=patience, trace=True, visit_order=visit_order)
+                       patience=patience, trace=True, visit_order=visit_order, probe_heads=probe_heads)
     ob = r["blocks_used"]
     gb = np.asarray(gpu_bu)[its]
     ties = 0

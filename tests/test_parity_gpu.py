@@ -306,3 +306,23 @@ def test_random_shapes(seed, monkeypatch):
     out, _, st, _ = run_gpu(w, "dense", dev=dev)
     assert st == 0
     check_dense(w, out, what=f"random case {seed} dense")
+
+
+@pytest.mark.parametrize("k", [2, 3, 5])
+def test_probe_heads_option(small, k, monkeypatch):
+    """art_decode_ex with the probe formed by the first 1, 2 or G query heads of
+    each group, against the oracle with the same option, for the kernel
+    variants (one and three consumer groups)."""
+    import kv_cache_early_gb300 as K
+    w = small[k]
+    for groups in ("1", "3"):
+        monkeypatch.setenv("ART_GROUPS", groups)
+        for ph in sorted({1, 2, w.group}):
+            dev = K.DeviceInputs(w)
+            dev.blocks_used.fill_(-7)
+            dev.art(1e-2, 1e-2, 2, probe_heads=ph)
+            torch.cuda.synchronize()
+            assert dev.status() == 0
+            out = dev.out.float().cpu().numpy().reshape(w.num_items, w.group, w.head_dim)
+            bu = dev.blocks_used.cpu().numpy().reshape(-1)
+            check_art(w, out, bu, 1e-2, 1e-2, 2, what=f"probe heads {ph}, groups {groups}", probe_heads=ph)
