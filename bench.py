@@ -363,16 +363,20 @@ def run_ours(args):
         dense["detector_overhead_frac"] = ms_z / ms_d - 1.0
 
     # roofline of the decode kernel (bytes actually needed by the blocks processed)
+    path = K.art_decode_path(dev.shape, p, dev.workspace.numel())
+    kernels = "art_units_kernel + art_units_combine" if path == 1 else "art_decode_kernel"
     peak, peak_kind = load_peaks()
     alg = kv_bytes(w, bu) + side_bytes(w)
     achieved = alg / (ms_kernel * 1e-3) / 1e9
     traffic, traffic_src = load_traffic(w.name, alg)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "traffic_source": traffic_src, "peak_kind": peak_kind,
-                "kernel": "art_decode_kernel", "algorithmic_bytes_per_launch": alg,
+                "kernel": kernels, "path": "units" if path == 1 else "one CTA per item",
+                "algorithmic_bytes_per_launch": alg,
                 "kernel_ms_per_launch": ms_kernel,
                 "kernel_ms_median_min_max": [float(np.median(t_kern)), float(t_kern.min()), float(t_kern.max())],
-                "timed": "decode kernel alone, CUDA events recorded by libart around its launch",
+                "timed": "decode kernel(s) alone, CUDA events recorded by libart around the launch "
+                         "(the unit path: the unit kernel and the merge kernel)",
                 "call_achieved_gbs": alg / (ms * 1e-3) / 1e9}
 
     # end to end through the public API with host buffers: per step the step's
@@ -453,7 +457,7 @@ def run_ours(args):
                 "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
                 "config": config_dict(w, eps, p, ws),
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
-                "gpu_launches": 2 * args.steps,
+                "gpu_launches": (3 if path == 1 else 2) * args.steps,
                 "dense_twin": dense,
                 "selection": selection,
                 "blocks_used": {"mean": float(bu.mean()), "listed_mean": float(n.mean()),

@@ -106,8 +106,28 @@ enum {
 };
 
 /* Bytes of device workspace art_decode / dense_decode need for `shape`.
- * Returns 0 if shape is NULL. */
+ * Returns 0 if shape is NULL. For bf16 with batch * num_kv_heads <= 256 this
+ * includes the area of the unit path (art_decode_path), which grows with
+ * max_pages_per_seq * page_size (the longest possible list). */
 size_t art_workspace_bytes(const art_shape* shape);
+
+/*
+ * Which kernel path art_decode takes for these arguments on the current device
+ * (an addition of this library; the ART paper describes one CTA per sequence):
+ *   0  one CTA per item (b, g): a persistent kernel whose CTAs claim whole
+ *      items, longest lists first;
+ *   1  the unit path: each item's list is cut into units of 16 blocks that
+ *      any CTA may take, so one item is spread over many SMs; the stop is
+ *      found from per-unit statistics joined by a look-back, the blocks of
+ *      the stopping unit up to the stop are recomputed, and a second kernel
+ *      merges the units' partial outputs. Blocks of units claimed before the
+ *      stop was known are read and discarded.
+ * The unit path is taken for bf16 when batch * num_kv_heads is at most 256 and
+ * below the number of SMs / 2, patience <= 16 and workspace_bytes covers its
+ * area; the environment variable ART_UNITS=0 or 1 forces the choice where the
+ * path is offered. A shape that fails the argument checks returns 0.
+ */
+int art_decode_path(const art_shape* shape, int32_t patience, size_t workspace_bytes);
 
 /*
  * ART decode attention (the method of the ART paper, sec. 3; the rule of the
@@ -117,7 +137,7 @@ size_t art_workspace_bytes(const art_shape* shape);
  * O^(i). It stops at the first i where `patience` consecutive tests passed
  * and logical block 0 (if listed) has been processed; blocks after i are
  * neither computed nor copied further (at most the blocks already in flight
- * are read).
+ * are read; on the unit path, art_decode_path, the units already claimed).
  *   eps_mag, eps_dir: thresholds tau and phi, >= 0 (+inf disables a test,
  *                     0 makes the test never pass)
  *   patience:         p >= 1

@@ -6,7 +6,7 @@
 #include <mutex>
 #include <string>
 
-#include "art_common.cuh"
+#include "art_units.cuh"
 
 namespace art {
 
@@ -26,16 +26,33 @@ struct PlanParams {
     int32_t* order;
     ItemInfo* info;
     int Hkv, Ps, max_pages, max_visit, m, D, num_pages, num_items;
+    // unit path (units != 0): its per-item and per-unit state, and the unit list;
+    // ctas = CTAs of the unit kernel (sets the unit length), patience = the call's
+    int units, maxk, ctas, patience;
+    int* p0;
+    int* stop_min;
+    int* resolved;
+    int* fail;
+    int* tflag;
+    int* uflags;
+    int2* ulist;
 };
 
 // One CTA per item: count the visit list (up to the first -1), check every
 // listed block and its pages, and record n and flags. The last CTA to finish
 // writes the claim order: items by visit-list length, longest first.
+// Unit path: each CTA also clears its item's unit state and records the list
+// position of block 0. The last CTA picks the unit length ck (8..16 blocks, at
+// least the patience) so that the units fill whole waves of the unit kernel's
+// CTAs, orders the items by units, and numbers the units round by round: unit
+// k of the items that have one, in claim order, then unit k + 1 (ck fix pieces
+// per item follow).
 __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams p) {
     __shared__ unsigned int bitmap[kBitmapWords];
     __shared__ int s_hist[kSortBuckets];
     __shared__ int s_part[kPlanThreads];
-    __shared__ int s_n, s_flags, s_last;
+    __shared__ int s_part2[kPlanThreads];
+    __shared__ int s_n, s_flags, s_last, s_p0;
     const int item = blockIdx.x, tid = threadIdx.x;
     const int b = item / p.Hkv;
     const int seq_len = p.seq_lens[b];
@@ -48,6 +65,7 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     if (tid == 0) {
         s_n = vrow ? p.max_visit : T;
         s_flags = 0;
+        s_p0 = 0x7fffffff;
     }
     __syncthreads();
     if (vrow)
@@ -63,7 +81,10 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
             err |= ART_STATUS_BAD_VISIT;
             continue;
         }
-        if (c == 0) has0 = 1;
+        if (c == 0) {
+            has0 = 1;
+            atomicMin(&s_p0, pos);
+        }
         if (dupcheck) {
             const unsigned int bit = 1u << (c & 31);
             if (atomicOr(&bitmap[c >> 5], bit) & bit) err |= ART_STATUS_DUP_VISIT;
@@ -89,6 +110,12 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     }
     if (has0) atomicOr(&s_flags, kItemHas0);
     if (err) atomicOr(&s_flags, err << 8);
+    if (p.units)
+        for (int k = tid; k < p.maxk; k += kPlanThreads) {
+            const size_t iu = (size_t)item * p.maxk + k;
+            p.tflag[iu] = 0;
+            reinterpret_cast<int4*>(p.uflags)[iu] = make_int4(0, 0, 0, 0);
+        }
     __syncthreads();
     if (tid == 0) {
         const int e = s_flags >> 8;
@@ -96,6 +123,12 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
         inf.n = n;
         inf.flags = (s_flags & kItemHas0) | (e ? kItemBad : 0);
         p.info[item] = inf;
+        if (p.units) {
+            p.p0[item] = (s_flags & kItemHas0) ? s_p0 : -1;
+            p.stop_min[item] = 0x7fffffff;
+            p.resolved[item] = 0;
+            p.fail[item] = 0;
+        }
         if (e) atomicOr(&p.hdr->status, e);
         __threadfence();
         s_last = (atomicAdd(&p.hdr->plan_done, 1u) == gridDim.x - 1) ? 1 : 0;
@@ -106,8 +139,40 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     // counting sort of the items by n, descending (buckets of n clamped at 4095)
     for (int i = tid; i < kSortBuckets; i += kPlanThreads) s_hist[i] = 0;
     __syncthreads();
+    // unit path: the unit length. With the lists' blocks spread over `ctas` CTAs in
+    // w waves of at most 16 blocks each, ck = total / (w ctas) rounded up, in 8..16
+    // and at least the patience (the count entering a unit then depends on the
+    // previous unit only)
+    __shared__ int s_ck;
+    if (p.units) {
+        int part = 0;
+        for (int it = tid; it < p.num_items; it += kPlanThreads) {
+            const int2 v = __ldcg(reinterpret_cast<const int2*>(&p.info[it]));
+            part += (v.y & kItemBad) ? 0 : v.x;
+        }
+        s_part2[tid] = part;
+        __syncthreads();
+        if (tid == 0) {
+            long long total = 0;
+            for (int i = 0; i < kPlanThreads; ++i) total += s_part2[i];
+            const long long cap = (long long)kUnitBlocks * p.ctas;
+            const long long waves = total > 0 ? (total + cap - 1) / cap : 1;
+            long long ck = (total + waves * p.ctas - 1) / (waves * p.ctas);
+            ck = ck < kUnitMinBlocks ? kUnitMinBlocks : ck > kUnitBlocks ? kUnitBlocks : ck;
+            if (ck < p.patience) ck = p.patience;
+            s_ck = (int)ck;
+            p.hdr->ck = (int)ck;
+        }
+        __syncthreads();
+    }
+    // sort key: the list length, or (unit path) the units of the list
+    auto sort_key = [&](int it) -> int {
+        const int2 v = __ldcg(reinterpret_cast<const int2*>(&p.info[it]));
+        if (!p.units) return v.x;
+        return (v.y & kItemBad) ? 0 : (v.x + s_ck - 1) / s_ck;
+    };
     for (int it = tid; it < p.num_items; it += kPlanThreads) {
-        const int nn = __ldcg(reinterpret_cast<const int*>(&p.info[it]));
+        const int nn = sort_key(it);
         atomicAdd(&s_hist[kSortBuckets - 1 - min(nn, kSortBuckets - 1)], 1);
     }
     __syncthreads();
@@ -133,10 +198,59 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     }
     __syncthreads();
     for (int it = tid; it < p.num_items; it += kPlanThreads) {
-        const int nn = __ldcg(reinterpret_cast<const int*>(&p.info[it]));
+        const int nn = sort_key(it);
         const int pos = atomicAdd(&s_hist[kSortBuckets - 1 - min(nn, kSortBuckets - 1)], 1);
         p.order[pos] = it;
     }
+    if (!p.units) return;
+    // unit path (num_items <= kPlanThreads): thread o holds claim position o
+    __syncthreads();
+    int* s_nch = s_part;
+    const int o = tid;
+    const int my_item = o < p.num_items ? __ldcg(&p.order[o]) : -1;
+    const int my_nch = o < p.num_items ? sort_key(my_item) : 0;
+    s_nch[o] = my_nch;
+    __syncthreads();
+    const int kmax = s_nch[0];  // units of the longest list (the order is by units, descending)
+    // cnt_k = items with more than k units = the first position whose item has <= k units
+    for (int k = tid; k < kmax; k += kPlanThreads) {
+        int lo = 0, hi = p.num_items;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_nch[mid] > k) lo = mid + 1; else hi = mid;
+        }
+        s_hist[k] = lo;
+    }
+    __syncthreads();
+    // S_k = units numbered before round k (exclusive prefix of cnt over 0 .. kmax - 1)
+    int chunk_sum = 0;
+    for (int i = 0; i < per; ++i) {
+        const int k = tid * per + i;
+        chunk_sum += k < kmax ? s_hist[k] : 0;
+    }
+    __syncthreads();
+    s_part2[tid] = chunk_sum;
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int i = 0; i < kPlanThreads; ++i) {
+            const int t = s_part2[i];
+            s_part2[i] = acc;
+            acc += t;
+        }
+        p.hdr->n_regular = acc;
+        p.hdr->n_units = acc + p.num_items * s_ck;  // then ck fix pieces per item
+    }
+    __syncthreads();
+    int acc = s_part2[tid];
+    for (int i = 0; i < per; ++i) {
+        const int k = tid * per + i;
+        const int t = k < kmax ? s_hist[k] : 0;
+        s_hist[k] = acc;
+        acc += t;
+    }
+    __syncthreads();
+    for (int k = 0; k < my_nch; ++k) p.ulist[s_hist[k] + o] = make_int2(my_item, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -187,6 +301,58 @@ static cudaError_t dispatch(const art_shape& s, const Params& p, cudaStream_t st
     return cudaErrorInvalidValue;
 }
 
+template <int D, int G>
+cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* li);
+
+static cudaError_t dispatch_units(const art_shape& s, const Params& p, const UParams& up, cudaStream_t st,
+                                  LaunchInfo* li) {
+    const int G = s.num_q_heads / s.num_kv_heads;
+#define ART_UCASE(DD, GG) \
+    if (s.head_dim == DD && G == GG) return launch_units<DD, GG>(p, up, st, li);
+#define ART_UCASES(DD) ART_UCASE(DD, 1) ART_UCASE(DD, 2) ART_UCASE(DD, 4) ART_UCASE(DD, 7) ART_UCASE(DD, 8)
+    ART_UCASES(128)
+    ART_UCASES(64)
+#undef ART_UCASES
+#undef ART_UCASE
+    return cudaErrorInvalidValue;
+}
+
+// The unit path (one item spread over many CTAs) is offered for bf16 with up to
+// kUnitMaxItems items; its workspace area is sized for the longest list the
+// block table allows.
+static int unit_maxk(const art_shape& s) {
+    const long long tmax = ((long long)s.max_pages_per_seq * s.page_size + kBK - 1) / kBK;
+    const long long k = (tmax + kUnitMinBlocks - 1) / kUnitMinBlocks;
+    return k > kUnitMaxK ? 0 : (int)k;
+}
+
+static bool unit_eligible(const art_shape& s) {
+    const long long items = (long long)s.batch * s.num_kv_heads;
+    return s.dtype == ART_DTYPE_BF16 && items <= kUnitMaxItems && unit_maxk(s) >= 1 && unit_maxk(s) < kUnitMaxK;
+}
+
+static size_t unit_area_offset(int num_items) { return align_up(workspace_bytes_for(num_items), 256); }
+
+static size_t unit_bytes(const art_shape& s) {
+    const int items = s.batch * s.num_kv_heads;
+    return make_unit_ws(items, unit_maxk(s), s.head_dim).total;
+}
+
+// Unit path or one CTA per item: ART_UNITS=0/1 forces the choice (where the
+// path is offered); otherwise the unit path runs when there are fewer items
+// than half the SMs.
+static bool want_units(const art_shape& s, int patience, size_t workspace_bytes) {
+    if (!unit_eligible(s) || patience > kUnitBlocks) return false;
+    const int items = s.batch * s.num_kv_heads;
+    if (workspace_bytes < unit_area_offset(items) + unit_bytes(s)) return false;
+    const char* env = std::getenv("ART_UNITS");
+    if (env) return std::atoi(env) != 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    return 2 * items < sms;
+}
+
 // events recorded around the decode-kernel launch of this thread's calls
 struct TimingEvents {
     cudaEvent_t start = nullptr, stop = nullptr;
@@ -224,6 +390,29 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     ItemInfo* info = reinterpret_cast<ItemInfo*>(hdr + 1);
     int32_t* order = reinterpret_cast<int32_t*>(info + num_items);
 
+    const bool units = kART && want_units(s, patience, workspace_bytes);
+    UParams up;
+    std::memset(&up, 0, sizeof up);
+    if (units) {
+        unsigned char* base = static_cast<unsigned char*>(workspace) + unit_area_offset(num_items);
+        const UnitWs w = make_unit_ws(num_items, unit_maxk(s), s.head_dim);
+        up.ulist = reinterpret_cast<const int2*>(base + w.ulist);
+        up.p0 = reinterpret_cast<const int*>(base + w.p0);
+        up.stop_min = reinterpret_cast<int*>(base + w.stop_min);
+        up.resolved = reinterpret_cast<int*>(base + w.resolved);
+        up.fail = reinterpret_cast<int*>(base + w.fail);
+        up.tflag = reinterpret_cast<int*>(base + w.tflag);
+        up.uflags = reinterpret_cast<int*>(base + w.uflags);
+        up.agg = reinterpret_cast<float*>(base + w.agg);
+        up.incl = reinterpret_cast<float*>(base + w.incl);
+        up.part_o = reinterpret_cast<float*>(base + w.part_o);
+        up.part_ml = reinterpret_cast<float*>(base + w.part_ml);
+        up.fix_o = reinterpret_cast<float*>(base + w.fix_o);
+        up.fix_ml = reinterpret_cast<float*>(base + w.fix_ml);
+        up.ck = 0;  // chosen on the device by the plan kernel
+        up.maxk = unit_maxk(s);
+    }
+
     cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
     if (e != cudaSuccess) return cuda_fail(e);
     PlanParams pp;
@@ -242,6 +431,24 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     pp.D = s.head_dim;
     pp.num_pages = s.num_pages_total;
     pp.num_items = num_items;
+    pp.units = units ? 1 : 0;
+    pp.maxk = up.maxk;
+    pp.patience = patience;
+    pp.ctas = 0;
+    if (units) {
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        pp.ctas = 2 * sms;  // the unit kernel runs two CTAs per SM
+    }
+    pp.p0 = const_cast<int*>(up.p0);
+    pp.stop_min = up.stop_min;
+    pp.resolved = up.resolved;
+    pp.fail = up.fail;
+    pp.tflag = up.tflag;
+    pp.uflags = up.uflags;
+    pp.ulist = const_cast<int2*>(up.ulist);
     art_plan_kernel<<<num_items, kPlanThreads, 0, st>>>(pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
 
@@ -274,7 +481,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     p.ph = probe_heads > 0 ? probe_heads : s.num_q_heads / s.num_kv_heads;
     p.tma3d = 0;
     if (t_events.start && (e = cudaEventRecord(t_events.start, st)) != cudaSuccess) return cuda_fail(e);
-    e = dispatch<kART>(s, p, st, env_stages(), li);
+    e = units ? dispatch_units(s, p, up, st, li) : dispatch<kART>(s, p, st, env_stages(), li);
     if (e != cudaSuccess) return cuda_fail(e);
     if (t_events.stop && (e = cudaEventRecord(t_events.stop, st)) != cudaSuccess) return cuda_fail(e);
     return ART_OK;
@@ -288,7 +495,14 @@ extern "C" {
 
 size_t art_workspace_bytes(const art_shape* shape) {
     if (!shape || shape->batch < 1 || shape->num_kv_heads < 1) return 0;
-    return workspace_bytes_for(shape->batch * shape->num_kv_heads);
+    const int items = shape->batch * shape->num_kv_heads;
+    if (check_shape(shape) == ART_OK && unit_eligible(*shape)) return unit_area_offset(items) + unit_bytes(*shape);
+    return workspace_bytes_for(items);
+}
+
+int art_decode_path(const art_shape* shape, int32_t patience, size_t workspace_bytes) {
+    if (check_shape(shape) != ART_OK) return 0;
+    return want_units(*shape, patience, workspace_bytes) ? 1 : 0;
 }
 
 int art_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,

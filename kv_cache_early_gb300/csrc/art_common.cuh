@@ -31,7 +31,11 @@ struct WsHeader {
     int status;              // ART_STATUS_* bits
     int check_code;          // first failed internal check (0 = none)
     int check_info[4];       // its details
-    int pad[8];
+    unsigned int uclaim;     // unit path: next unit to hand out
+    int n_regular;           // unit path: units of the visit lists (the fix units follow)
+    int n_units;             // unit path: all units
+    int ck;                  // unit path: ART blocks per unit, chosen by the plan kernel
+    int pad[4];
 };
 
 // Host: keeps the text of a failed CUDA call for art_last_cuda_error and returns ART_ERR_LAUNCH.

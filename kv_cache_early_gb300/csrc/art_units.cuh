@@ -1,0 +1,1290 @@
+// art_units.cuh -- ART decode attention with one item spread over many CTAs.
+//
+// With fewer items (sequence b, KV head g) than SMs, one CTA per item leaves
+// most SMs idle, and an item runs no faster than one SM streams. Here each
+// item's visit list is cut into units of `ck` consecutive entries that any CTA
+// may take:
+//
+//   plan        numbers the units round by round (unit k of every item, longest
+//               lists first, before unit k + 1 of any item), then ck fix pieces
+//               per item; CTAs claim units in that order from a counter.
+//   producer    TMA copies of a unit's blocks (with the queries at its first
+//               block) into the ring of shared-memory slots.
+//   consumers   softmax attention of each block for the G query heads (tensor
+//               cores, the 64 keys split over 4 warps, as in the one-CTA
+//               kernel), folded into the unit's partial output (per warp: a
+//               running max, weight sum and output sums), which goes to global
+//               memory at the unit's end; each block's probe partials go to the
+//               statistics warp.
+//   statistics  publishes the unit's probe aggregate (max, weight sum, probe
+//               sums per head) and takes the state of the probe before the unit
+//               from a look-back over the item's earlier units (their
+//               aggregates, back to the nearest one that has published its
+//               inclusive state). From that state it runs the stability test of
+//               each block of the unit in order, exactly as one pass over the
+//               list would (ART paper sec. 3.2; explainer sec. 2.2-2.4), and
+//               publishes the unit's stable bits. With patience <= ck the
+//               patience count entering a unit depends on the previous unit's
+//               bits only, so the unit can name its first stop position (if
+//               any) at once and lowers the item's stop to it (atomicMin).
+//               Every position before the one-pass stop sees the same
+//               statistics as the one-pass rule, so the smallest position named
+//               is that stop.
+//   fix pieces  ck per item, claimed after every unit: once every unit of the
+//               item has named its stop (or been skipped), piece j recomputes
+//               block j of the stopping unit if it lies at or before the stop
+//               (that unit's own partial also holds blocks after it), one block
+//               per CTA, so the recompute is spread over the GPU.
+//   combine     a second kernel merges, per item, the partials of the units
+//               before the stopping unit and of the fix pieces (or the stopping
+//               unit itself when it ends at the stop): O = sums / weight sums.
+//
+// A unit whose item has already stopped before it when it is claimed is
+// skipped; units claimed before the stop was known are read and discarded.
+//
+// A CTA waits on another CTA's unit only for a unit claimed earlier; every CTA
+// works through its units in claim order and the compute of a unit never
+// waits on another unit, so the waits end. They are bounded all the same.
+#pragma once
+
+#include "art_kernel.cuh"
+
+namespace art {
+
+constexpr int kUnitBlocks = 16;     // ck: ART blocks per unit at most
+constexpr int kUnitMinBlocks = 8;   // ... and at least (the workspace is sized for it)
+constexpr int kUnitMaxItems = 256;  // the unit path is offered up to this many items
+constexpr int kUnitMaxK = 4096;     // units per item at most
+constexpr int kUnitWords = 10;      // words per lane of a probe state: max, weight sum, 8 probe slots
+
+// Global-memory flags between CTAs: release stores, acquire loads (GPU scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// atomic add with release semantics: this thread's earlier writes are visible first
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Byte offsets of the unit path's workspace area (after the one-CTA path's).
+struct UnitWs {
+    size_t p0, stop_min, resolved, fail, ulist, tflag, uflags, agg, incl, part_o, part_ml, fix_o, fix_ml, total;
+};
+
+__host__ __device__ inline UnitWs make_unit_ws(int items, int maxk, int D) {
+    UnitWs w;
+    const size_t U = (size_t)items * maxk;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    w.p0 = take((size_t)items * 4);
+    w.stop_min = take((size_t)items * 4);
+    w.resolved = take((size_t)items * 4);
+    w.fail = take((size_t)items * 4);
+    w.ulist = take(U * 8);
+    w.tflag = take(U * 4);
+    w.uflags = take(U * 16);
+    w.agg = take(U * 32 * kUnitWords * 4);
+    w.incl = take(U * 32 * kUnitWords * 4);
+    w.part_o = take(U * 32 * (size_t)D * 4);
+    w.part_ml = take(U * 64 * 4);
+    w.fix_o = take((size_t)items * kUnitBlocks * 32 * D * 4);
+    w.fix_ml = take((size_t)items * kUnitBlocks * 64 * 4);
+    w.total = o;
+    return w;
+}
+
+struct UParams {
+    const int2* ulist;  // claim position -> (item, unit index k)
+    const int* p0;      // per item: list position of logical block 0, or -1
+    int* stop_min;      // per item: smallest stop position named so far
+    int* resolved;      // per item: units whose stop is named (or that were skipped)
+    int* fail;          // per item: a page check failed in this path
+    int* tflag;         // per (item, k): 1 aggregate, 2 and inclusive state, 3 skipped
+    int* uflags;        // per (item, k): {stable bits, blocks, state (1 set, 3 skipped), 0}
+    float* agg;         // per (item, k): [kUnitWords][32 lanes] probe state of the unit's blocks
+    float* incl;        // per (item, k): the same through the unit (from the list's start)
+    float* part_o;      // per (item, k): [4 warps][32 lanes][D / 4] output sums (mma fragment order)
+    float* part_ml;     // per (item, k): [4 warps][2][8] running max, weight sum per head column
+    float* fix_o;       // per (item, fix piece): the piece's partial, same layout
+    float* fix_ml;
+    int ck;             // ART blocks per unit (the kernels take it from the workspace header)
+    int maxk;           // units per item at most
+};
+
+enum UnitKind : int { kUBlock = 0, kUFix = 1, kUEnd = 2 };
+
+struct UMeta {
+    int kind, item, k, j, nj, pos, n, c, nvalid, b, g, pad;
+};
+
+struct URec {
+    int kind, item, k, j, nj, pad0, pad1, pad2;
+};
+
+template <int D, int G>
+struct UCfg {
+    using C = Cfg<true, D, G, 1>;
+    static constexpr int THREADS = 6 * 32;  // 4 consumer warps, producer, statistics
+    static constexpr int W = C::SPL + 2;
+    static_assert(W <= kUnitWords, "probe state fits the workspace words");
+};
+
+struct ULayout {
+    size_t meta, bars, part, plb, pmb, qt, ptab, rinfo, ust, ctrl, total;
+};
+
+template <int D, int G>
+__host__ __device__ inline ULayout make_ulayout(int stages) {
+    using C = typename UCfg<D, G>::C;
+    ULayout L;
+    size_t o = (size_t)stages * C::SLOT;
+    L.meta = o;
+    o += (size_t)stages * sizeof(UMeta);
+    o = align_up(o, 16);
+    L.bars = o;  // full[stages], empty[stages], part_full[NB], part_empty[NB]
+    o += (size_t)(2 * stages + 2 * C::NB) * sizeof(uint64_t);
+    o = align_up(o, 16);
+    L.part = o;  // [NB][4 warps][PRW][PST] probe partial rows
+    o += (size_t)C::NB * C::GW * C::PRW * C::PST * sizeof(float);
+    L.plb = o;  // [NB][4][G] block weight sums
+    o += (size_t)C::NB * C::GW * G * sizeof(float);
+    L.pmb = o;  // [NB][4][G] block maxima
+    o += (size_t)C::NB * C::GW * G * sizeof(float);
+    o = align_up(o, 1024);
+    L.qt = o;  // the unit's queries, 8 rows (heads past G zero), 128B-swizzled
+    o += (size_t)8 * C::ROWB;
+    L.ptab = o;  // rank of each head dim among the probe dims, or -1
+    o += (size_t)D * sizeof(int);
+    o = align_up(o, 16);
+    L.rinfo = o;
+    o += (size_t)C::NB * sizeof(URec);
+    o = align_up(o, 16);
+    L.ust = o;  // [ck][W][32 lanes] block summaries of the unit being tested
+    o += (size_t)kUnitBlocks * UCfg<D, G>::W * 32 * sizeof(float);
+    o = align_up(o, 16);
+    L.ctrl = o;
+    o += sizeof(Ctrl);
+    L.total = align_up(o, 128) + 1024;  // room to align the ring to 1024 bytes
+    return L;
+}
+
+// Polls a global flag until it is >= want (the value read goes to `got`);
+// false when this CTA gave up elsewhere or after kWaitLimitNs. Every lane
+// then loads the flag once more with acquire semantics, so each lane's later
+// loads of the payload are ordered after it.
+__device__ __forceinline__ bool poll_flag(const int* flag, int want, int& got, Ctrl* ctrl, WsHeader* hdr,
+                                          int where) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0;; ++it) {
+        int v = 0;
+        if (lane == 0) v = ld_acquire_gpu(flag);
+        v = __shfl_sync(0xffffffffu, v, 0);
+        if (v >= want) {
+            got = ld_acquire_gpu(flag);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            return true;
+        }
+        int quit = 0;
+        if (lane == 0) {
+            if (ld_volatile_shared(&ctrl->abort)) quit = 1;
+            else if ((it & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+                st_volatile_shared(&ctrl->abort, 1);
+                atomicOr(&hdr->status, ART_STATUS_TIMEOUT);
+                record_check(hdr, where, want, v, 0);
+                quit = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, quit, 0)) return false;
+        __nanosleep(64);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// producer warp
+// ---------------------------------------------------------------------------
+template <class C>
+__device__ void producer_u(const Params& p, const UParams& up, unsigned char* ring, UMeta* meta, uint64_t* full,
+                           uint64_t* empty, Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv) {
+    constexpr int G = C::GQ;
+    constexpr int NH = C::ROWB / 128;
+    const int lane = threadIdx.x & 31;
+    int slot = 0;
+    uint32_t round = 0;
+    unsigned long long issued = 0;
+    bool ok = true;
+    const int n_reg = p.hdr->n_regular, n_units = p.hdr->n_units;  // written by the plan kernel
+
+    auto acquire = [&]() -> bool { return wait_bounded(&empty[slot], (round & 1u) ^ 1u, ctrl, p.hdr, 231); };
+    auto advance = [&]() {
+        ++issued;
+        if (++slot == p.stages) {
+            slot = 0;
+            ++round;
+        }
+    };
+    // a unit that will not be computed: mark it for the look-backs and the stop count
+    auto mark_skipped = [&](int item, int k) {
+        const size_t iu = (size_t)item * up.maxk + k;
+        if (lane == 0) {
+            st_release_gpu(&up.tflag[iu], 3);
+            st_release_gpu(&up.uflags[4 * iu + 2], 3);
+            red_release_add(&up.resolved[item], 1);
+        }
+        __syncwarp();
+    };
+
+    for (;;) {
+        int u = 0;
+        if (lane == 0) u = (int)atomicAdd(&p.hdr->uclaim, 1u);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= n_units) {
+            // nothing left to claim: the merge kernel may be launched
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            if (!acquire()) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                UMeta& mt = meta[slot];
+                mt.kind = kUEnd; mt.item = -1; mt.k = 0; mt.j = 0; mt.nj = 1; mt.pos = 0; mt.n = 0; mt.c = -1;
+                mt.nvalid = 0; mt.b = 0; mt.g = 0;
+                mbar_arrive(&full[slot]);
+            }
+            __syncwarp();
+            advance();
+            break;
+        }
+        const bool fix = u >= n_reg;
+        int item, k = 0;
+        if (!fix) {
+            const int2 e = up.ulist[u];
+            item = e.x;
+            k = e.y;
+        } else {
+            const int f = u - n_reg;  // fix piece f % ck of the item at claim position f / ck
+            item = p.order[f / up.ck];
+            k = f % up.ck;
+        }
+        if (item < 0 || item >= p.num_items) {
+            if (lane == 0) record_check(p.hdr, 201, u, item, 0);
+            continue;
+        }
+        const ItemInfo inf = p.info[item];
+        const int n = (inf.flags & kItemBad) ? 0 : inf.n;
+        const int nch = (n + up.ck - 1) / up.ck;
+        const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
+        int first = 0, cnt = 0;
+        if (fix) {
+            if (nch == 0) continue;
+            int got = 0;
+            if (!poll_flag(&up.resolved[item], nch, got, ctrl, p.hdr, 232)) {
+                ok = false;
+                break;
+            }
+            if (ld_acquire_gpu(&up.fail[item])) continue;
+            const int t = ld_acquire_gpu(&up.stop_min[item]);
+            if (t < 0 || t >= n) {
+                if (lane == 0) record_check(p.hdr, 233, item, t, n);
+                continue;
+            }
+            const int sfirst = t / up.ck * up.ck;
+            if (t == min(n, sfirst + up.ck) - 1) continue;  // the stopping unit ends at the stop
+            if (sfirst + k > t) continue;                   // this piece's block lies past the stop
+            first = sfirst + k;
+            cnt = 1;
+        } else {
+            if (k < 0 || k >= nch) {
+                if (lane == 0) record_check(p.hdr, 234, item, k, nch);
+                continue;
+            }
+            first = k * up.ck;
+            cnt = min(up.ck, n - first);
+            if (ld_acquire_gpu(&up.stop_min[item]) < first) {
+                mark_skipped(item, k);
+                continue;
+            }
+        }
+        // each lane resolves one listed position of the unit (cnt <= 32)
+        const int seq_len = p.seq_lens[b];
+        const int32_t* trow = p.block_table + (size_t)b * p.max_pages;
+        const int32_t* vrow = p.visit ? p.visit + (size_t)item * p.max_visit : nullptr;
+        int c = 0, nvalid = 0, npv = 0, bad = 0, r0 = 0;
+        int pg[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pg[q] = 0;
+        if (lane < cnt) {
+            const int pos = first + lane;
+            c = vrow ? vrow[pos] : pos;
+            const int t0 = c * kBK;
+            if (c < 0 || t0 >= seq_len) {
+                bad = 1;
+            } else {
+                nvalid = min(kBK, seq_len - t0);
+                if (p.Ps <= kBK) {
+                    npv = (nvalid + p.Ps - 1) / p.Ps;
+                    const int pfirst = t0 / p.Ps;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q < npv) pg[q] = trow[pfirst + q];
+                } else {
+                    npv = 1;
+                    pg[0] = trow[t0 / p.Ps];
+                    r0 = t0 % p.Ps;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < npv && (pg[q] < 0 || pg[q] >= p.num_pages)) bad = 1;
+            }
+        }
+        if (__any_sync(0xffffffffu, bad)) {
+            if (lane == 0) {
+                atomicOr(&p.hdr->status, ART_STATUS_BAD_PAGE);
+                atomicExch(&up.fail[item], 1);
+            }
+            if (!fix) mark_skipped(item, k);
+            continue;
+        }
+        for (int j = 0; j < cnt; ++j) {
+            if (!acquire()) {
+                ok = false;
+                break;
+            }
+            const int cj = __shfl_sync(0xffffffffu, c, j);
+            const int nvj = __shfl_sync(0xffffffffu, nvalid, j);
+            const int npj = __shfl_sync(0xffffffffu, npv, j);
+            const int r0j = __shfl_sync(0xffffffffu, r0, j);
+            int pgj[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pgj[q] = __shfl_sync(0xffffffffu, pg[q], j);
+            const bool with_q = j == 0;
+            const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
+            const uint32_t page_bytes = (uint32_t)(page_rows * C::ROWB);
+            const uint32_t bytes = 2u * npj * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
+            unsigned char* dst = ring + (size_t)slot * C::SLOT;
+            if (lane == 0) {
+                UMeta& mt = meta[slot];
+                mt.kind = fix ? kUFix : kUBlock; mt.item = item; mt.k = k; mt.j = j; mt.nj = cnt;
+                mt.pos = first + j; mt.n = n; mt.c = cj; mt.nvalid = nvj; mt.b = b; mt.g = g;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+            }
+            __syncwarp();
+            // each page's rows land as [column half][rows][128 B] (128B-swizzled), pages one
+            // after another; one 3-D copy per page, or one 2-D copy per column half
+            const int nop = p.tma3d ? npj : npj * NH;
+            const int nbox = 2 * nop;
+            for (int t = lane; t < nbox + (with_q ? 1 : 0); t += 32) {
+                if (t < nbox) {
+                    const int kv = t / nop;
+                    const int rem = t - kv * nop;
+                    const int q = p.tma3d ? rem : rem / NH, hf = p.tma3d ? 0 : rem - (rem / NH) * NH;
+                    int pk = 0;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        if (x == q) pk = pgj[x];
+                    const int y = (pk * p.Hkv + g) * p.Ps + r0j;
+                    unsigned char* d = dst + kv * C::KVB + (q * NH + hf) * page_rows * 128;
+                    if (p.tma3d)
+                        tma_load_3d(d, kv ? tv : tk, 0, y, 0, &full[slot]);
+                    else
+                        tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
+                } else {
+                    const char* src = static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
+                    bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
+                }
+            }
+            __syncwarp();
+            advance();
+        }
+        if (!ok) break;
+    }
+
+    if (!ok) {
+        // aborting: wait (bounded) for this CTA's own copies still in flight
+        const unsigned long long lim = issued < (unsigned long long)p.stages ? issued : p.stages;
+        int s = slot;
+        uint32_t r = round;
+        for (unsigned long long q = 0; q < lim; ++q) {
+            if (--s < 0) {
+                s = p.stages - 1;
+                --r;
+            }
+            const unsigned long long t0 = global_ns();
+            while (!__all_sync(0xffffffffu, mbar_try_wait(&full[s], r & 1u)) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps (one group of 4; warp wg owns keys 16 wg .. 16 wg + 15 of a block)
+// ---------------------------------------------------------------------------
+template <class C>
+__device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ring, const UMeta* meta,
+                           uint64_t* full, uint64_t* empty, uint64_t* part_full, uint64_t* part_empty, URec* rinfo,
+                           const ULayout& L, unsigned char* smem, const int* prank, Ctrl* ctrl) {
+    constexpr int G = C::GQ, D = C::DD, KS = C::KS, GW = C::GW, NB = C::NB;
+    constexpr bool SPLITN = C::SPLITN;
+    const int wg = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 2, tig = lane & 3;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    const bool v0 = h0 < G, v1 = h1 < G;  // the score columns of this lane hold real heads
+    // O^T columns of this lane: heads (q0, q1); with the split tile, lanes with tig >= 2
+    // hold the low parts of heads 2 tig - 4, 2 tig - 3
+    const bool lo_lane = SPLITN && tig >= 2;
+    const int q0 = lo_lane ? h0 - 4 : h0, q1 = q0 + 1;
+    const bool u0 = q0 < G, u1 = q1 < G;
+    const bool w0 = u0 && !lo_lane, w1 = u1 && !lo_lane;
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    float* plb = reinterpret_cast<float*>(smem + L.plb);
+    float* pmb = reinterpret_cast<float*>(smem + L.pmb);
+    unsigned char* sQt = smem + L.qt;
+    const uint32_t qtbase = smem_addr(sQt);
+    const float scale = 1.4426950408889634f / sqrtf((float)D);
+    const int gtid = threadIdx.x;  // 0 .. 127
+    // this lane's O^T rows are d = 16 mt + grp + 8 r; bit 2 mt + r marks a probe dim,
+    // byte 2 mt + r of prk holds its rank among the probe dims
+    uint32_t pbits = 0;
+    uint32_t prk[(2 * KS + 3) / 4];
+#pragma unroll
+    for (int i = 0; i < (2 * KS + 3) / 4; ++i) prk[i] = 0;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int rk = prank[16 * mt + grp + 8 * r];
+            if (rk >= 0) {
+                pbits |= 1u << (2 * mt + r);
+                prk[(2 * mt + r) >> 2] |= (uint32_t)rk << (8 * ((2 * mt + r) & 3));
+            }
+        }
+    const int mi = lane >> 3, lr = lane & 7;
+    const int keyK = wg * 16 + (mi & 1) * 8 + lr;   // K rows for the S^T A fragments
+    const int chK = mi >> 1;
+    const int keyV = wg * 16 + (mi >> 1) * 8 + lr;  // V rows for the O^T A fragments
+    const int chV = mi & 1;
+    const int PR = p.Ps < kBK ? p.Ps : kBK;
+    const int lpr = 31 - __clz(PR);
+    auto rowoff = [=](int row) -> uint32_t {
+        return (uint32_t)(((row >> lpr) * (C::ROWB / 128) * PR + (row & (PR - 1))) * 128);
+    };
+    auto sw = [=](uint32_t base, int row, int chunk) -> uint32_t {
+        return base + rowoff(row) + (uint32_t)((chunk >> 3) * PR * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    };
+
+    float acc[KS][4], tN[KS][4];
+    float mrun[2], lrun[2], mbN[2], lbN[2];
+    auto reset = [&]() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mrun[j] = -INFINITY;
+            lrun[j] = 0.f;
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
+    };
+    reset();
+    mbN[0] = mbN[1] = lbN[0] = lbN[1] = 0.f;
+    auto fold = [&]() {
+        float a[2], bb[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const bool none = mbN[j] == -INFINITY;  // a head beyond G, or no valid key: keep the state
+            const float mn = none ? mrun[j] : fmaxf(mrun[j], mbN[j]);
+            a[j] = none ? 1.f : exp2f(mrun[j] - mn);
+            bb[j] = none ? 0.f : exp2f(mbN[j] - mn);
+            lrun[j] = none ? lrun[j] : a[j] * lrun[j] + bb[j] * lbN[j];
+            mrun[j] = mn;
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][c] = a[c & 1] * acc[mt][c] + bb[c & 1] * tN[mt][c];
+    };
+    int rec = 0;  // records published to the statistics warp
+    auto publish = [&](const UMeta& mt, int kind, bool data) -> bool {
+        const int rb = rec % NB;
+        if (rec >= NB && !wait_bounded(&part_empty[rb], (uint32_t)(rec / NB - 1) & 1u, ctrl, p.hdr, 242))
+            return false;
+        if (data) {
+            float* pp = part + (((size_t)rb * GW + wg) * C::PRW + (lo_lane ? 1 : 0)) * C::PST + q0;
+#pragma unroll
+            for (int m = 0; m < KS; ++m)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const bool on = (pbits >> (2 * m + r)) & 1u;
+                    const int rank = (int)((prk[(2 * m + r) >> 2] >> (8 * ((2 * m + r) & 3))) & 0xffu);
+                    float* dst = pp + rank * C::GP;
+                    if (G >= 2) st_shared_if(on && u1, dst, tN[m][2 * r], tN[m][2 * r + 1]);
+                    if (G % 2) st_shared_if(on && u0 && !u1, dst, tN[m][2 * r]);
+                }
+            st_shared_if(grp == 0 && w0, &plb[(rb * GW + wg) * G + (w0 ? q0 : 0)], lbN[0]);
+            st_shared_if(grp == 0 && w1, &plb[(rb * GW + wg) * G + (w1 ? q1 : 0)], lbN[1]);
+            st_shared_if(grp == 0 && w0, &pmb[(rb * GW + wg) * G + (w0 ? q0 : 0)], mbN[0]);
+            st_shared_if(grp == 0 && w1, &pmb[(rb * GW + wg) * G + (w1 ? q1 : 0)], mbN[1]);
+        }
+        if (wg == 0 && lane == 0) {
+            URec& r = rinfo[rb];
+            r.kind = kind; r.item = mt.item; r.k = mt.k; r.j = mt.j; r.nj = mt.nj;
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, &part_full[rb]);
+        ++rec;
+        return true;
+    };
+    // the unit's partial: output sums in mma fragment order, then max and weight sum per head
+    auto write_partial = [&](const UMeta& mt) {
+        float* po;
+        float* pml;
+        if (mt.kind == kUFix) {
+            const size_t ip = (size_t)mt.item * up.ck + mt.k;
+            po = up.fix_o + ip * 32 * D;
+            pml = up.fix_ml + ip * 64;
+        } else {
+            const size_t iu = (size_t)mt.item * up.maxk + mt.k;
+            po = up.part_o + iu * 32 * D;
+            pml = up.part_ml + iu * 64;
+        }
+        if constexpr (SPLITN) {
+            // high + low parts (both lanes carry the same running max and sum)
+#pragma unroll
+            for (int m = 0; m < KS; ++m)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[m][c] += __shfl_xor_sync(0xffffffffu, acc[m][c], 2);
+        }
+        float4* dst = reinterpret_cast<float4*>(po + ((size_t)wg * 32 + lane) * (KS * 4));
+#pragma unroll
+        for (int m = 0; m < KS; ++m) dst[m] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+        if (grp == 0) {
+            if (w0) {
+                pml[wg * 16 + q0] = mrun[0];
+                pml[wg * 16 + 8 + q0] = lrun[0];
+            }
+            if (w1) {
+                pml[wg * 16 + q1] = mrun[1];
+                pml[wg * 16 + 8 + q1] = lrun[1];
+            }
+        }
+    };
+
+    for (int e = 0;; ++e) {
+        const int slot = e % p.stages;
+        if (!wait_bounded(&full[slot], (uint32_t)(e / p.stages) & 1u, ctrl, p.hdr, 241)) return;
+        const UMeta mt = meta[slot];
+        const bool valid =
+            mt.kind == kUEnd ||
+            ((mt.kind == kUBlock || mt.kind == kUFix) && mt.item >= 0 && mt.item < p.num_items && mt.nvalid >= 1 &&
+             mt.nvalid <= kBK && mt.nj >= 1 && mt.nj <= up.ck && mt.j >= 0 && mt.j < mt.nj && mt.k >= 0 &&
+             mt.k < (mt.kind == kUFix ? up.ck : up.maxk) && mt.b >= 0 && mt.b < p.B && mt.g >= 0 && mt.g < p.Hkv);
+        if (!valid || mt.kind == kUEnd) {
+            if (!valid && lane == 0) record_check(p.hdr, 243, e, mt.kind, mt.item);
+            __syncwarp();
+            mbar_arrive_if(lane == 0, &empty[slot]);
+            UMeta endm = mt;
+            publish(endm, kUEnd, false);
+            return;
+        }
+        unsigned char* sK = ring + (size_t)slot * C::SLOT;
+        unsigned char* sV = sK + C::KVB;
+        if (mt.j == 0) {
+            // the unit's queries into the swizzled 8-row area (rows past G zero), once every
+            // warp has finished the previous block's scores
+            reset();
+            named_bar_sync(1, GW * 32);
+            const unsigned char* sQ = sK + 2 * C::KVB;
+            constexpr int QCH = 8 * (C::ROWB / 16);
+            for (int i = gtid; i < QCH; i += GW * 32) {
+                const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
+            }
+            named_bar_sync(1, GW * 32);
+        }
+        const int nvalid = mt.nvalid;
+        // ---- S^T for this warp's 16 keys (two independent accumulation chains)
+        float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t kbase = smem_addr(sK), vbase = smem_addr(sV);
+        __syncwarp();
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp) {
+            uint32_t b00, b01, b10, b11;
+            {
+                const int c = 4 * kp + mi;
+                ldsm_x4(qtbase + (uint32_t)((c >> 3) * 1024 + lr * 128 + (((c & 7) ^ lr) << 4)), b00, b01, b10, b11);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ks = 2 * kp + h;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sw(kbase, keyK, 2 * ks + chK), a0, a1, a2, a3);
+                mma_bf16(h ? s4b : s4, a0, a1, a2, a3, h ? b10 : b00, h ? b11 : b01);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s4[c] += s4b[c];
+        const int k0 = wg * 16 + grp, k1 = k0 + 8;
+        float sc[4];
+        sc[0] = (k0 < nvalid && v0) ? s4[0] * scale : -INFINITY;
+        sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
+        sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
+        sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
+        // ---- this warp's block max per head (each warp keeps its own running max)
+        float mb0 = fmaxf(sc[0], sc[2]), mb1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            mb0 = fmaxf(mb0, __shfl_xor_sync(0xffffffffu, mb0, o));
+            mb1 = fmaxf(mb1, __shfl_xor_sync(0xffffffffu, mb1, o));
+        }
+        float pw[4];
+        pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mb0);
+        pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mb1);
+        pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - mb0);
+        pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - mb1);
+        float l0 = pw[0] + pw[2], l1 = pw[1] + pw[3];
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        if constexpr (SPLITN) {
+            // low-part lanes take the weights, maxima and sums of lane ^ 2
+            float px[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) px[c] = __shfl_xor_sync(0xffffffffu, pw[c], 2);
+            const float mx0 = __shfl_xor_sync(0xffffffffu, mb0, 2), mx1 = __shfl_xor_sync(0xffffffffu, mb1, 2);
+            const float lx0 = __shfl_xor_sync(0xffffffffu, l0, 2), lx1 = __shfl_xor_sync(0xffffffffu, l1, 2);
+            float t[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) t[c] = lo_lane ? px[c] : pw[c];
+            mbN[0] = lo_lane ? mx0 : mb0;
+            mbN[1] = lo_lane ? mx1 : mb1;
+            lbN[0] = lo_lane ? lx0 : l0;
+            lbN[1] = lo_lane ? lx1 : l1;
+            const uint32_t hA = pack_bf16(t[0], t[1]), hB = pack_bf16(t[2], t[3]);
+            const uint32_t lA = pack_bf16(t[0] - bf16_lo_f(hA), t[1] - bf16_hi_f(hA));
+            const uint32_t lB = pack_bf16(t[2] - bf16_lo_f(hB), t[3] - bf16_hi_f(hB));
+            __syncwarp();
+            bh0 = movm_t(lo_lane ? lA : hA);
+            bh1 = movm_t(lo_lane ? lB : hB);
+        } else {
+            mbN[0] = mb0;
+            mbN[1] = mb1;
+            lbN[0] = l0;
+            lbN[1] = l1;
+            const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
+            const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
+            const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
+            __syncwarp();
+            bh0 = movm_t(hA);
+            bh1 = movm_t(hB);
+            bl0 = movm_t(lA);
+            bl1 = movm_t(lB);
+        }
+        // ---- rows past the sequence end hold stale data: zero this warp's, so 0 * V stays 0
+        if (nvalid < wg * 16 + 16) {
+            const int r0 = max(nvalid, wg * 16);
+            const int nchunks = (wg * 16 + 16 - r0) * (C::ROWB / 16);
+            for (int i = lane; i < nchunks; i += 32) {
+                const int row = r0 + i / (C::ROWB / 16), c = i % (C::ROWB / 16);
+                *reinterpret_cast<uint4*>(sV + rowoff(row) + (c >> 3) * PR * 128 + (c & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        // ---- O^T partial of this block
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < KS; ++m) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(sw(vbase, keyV, 2 * m + chV), a0, a1, a2, a3);
+            tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
+            mma_bf16(tN[m], a0, a1, a2, a3, bh0, bh1);
+            if constexpr (!SPLITN) mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, &empty[slot]);  // the slot's data are no longer read
+        if (mt.kind == kUBlock && !publish(mt, kUBlock, true)) return;
+        fold();
+        if (mt.j == mt.nj - 1) write_partial(mt);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// statistics warp
+// ---------------------------------------------------------------------------
+template <class C>
+__device__ void stat_u(const Params& p, const UParams& up, const float* part, const float* plb, const float* pmb,
+                       uint64_t* part_full, uint64_t* part_empty, const URec* rinfo, float* ust, Ctrl* ctrl) {
+    constexpr int G = C::GQ, SPL = C::SPL, NB = C::NB, RGW = C::RGW;
+    constexpr int NPR = C::RGW * C::PRW;  // partial rows per record
+    constexpr int W = SPL + 2;
+    constexpr int UW = 32 * kUnitWords;   // floats of one probe state in the workspace
+    const int lane = threadIdx.x & 31;
+    const int m = p.m;
+    // probe slot s = lane + 32 j is word s of a partial row: head s % GP, rank s / GP;
+    // heads from p.ph on are not part of the probe
+    int hs[SPL];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) {
+        const int s = lane + 32 * j;
+        hs[j] = (s % C::GP < p.ph && s / C::GP < m) ? s % C::GP : -1;
+    }
+    const int hme = lane % C::GP < G ? lane % C::GP : 0;  // this lane's slots all belong to head hme
+
+    float Ma = -INFINITY, La = 0.f, Oa[SPL];  // aggregate of the unit's blocks so far
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) Oa[j] = 0.f;
+
+    // (M1, L1, O1) <- merge with (M2, L2, O2): the same softmax state over both sets of blocks
+    auto merge = [&](float& M1, float& L1, float (&O1)[SPL], float M2, float L2, const float (&O2)[SPL]) {
+        if (M2 == -INFINITY) return;
+        const float Mn = fmaxf(M1, M2);
+        const float a = exp2f(M1 - Mn), bw = exp2f(M2 - Mn);
+        L1 = fmaf(a, L1, bw * L2);
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) O1[j] = fmaf(a, O1[j], bw * O2[j]);
+        M1 = Mn;
+    };
+
+    auto finish_unit = [&](int item, int k, int nj) -> bool {
+        const size_t iu = (size_t)item * up.maxk + k;
+        {
+            float* ga = up.agg + iu * UW;
+            ga[lane] = Ma;
+            ga[32 + lane] = La;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) ga[(2 + j) * 32 + lane] = Oa[j];
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(&up.tflag[iu], 1);
+        }
+        // the probe state before this unit: aggregates of the earlier units, back to the
+        // nearest one with an inclusive state
+        float cM = -INFINITY, cL = 0.f, cO[SPL];
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) cO[j] = 0.f;
+        bool dead = false;
+        {
+            // lane j reads the flag of unit kk - j; the lanes from 0 up to the first unit with an
+            // inclusive state (or a skip mark, or the list's start) whose states are published
+            // are folded together, their loads in flight at once
+            const size_t ibase = (size_t)item * up.maxk;
+            const unsigned long long t0 = global_ns();
+            int kk = k - 1;
+            for (unsigned it = 0; kk >= 0; ++it) {
+                const int uj = kk - lane;
+                const int fl = uj >= 0 ? ld_acquire_gpu(&up.tflag[ibase + uj]) : 2;  // before the list: empty
+                const unsigned pub = __ballot_sync(0xffffffffu, fl >= 1);
+                const unsigned endm = __ballot_sync(0xffffffffu, fl >= 2);
+                const int r = pub == 0xffffffffu ? 32 : __ffs(~pub) - 1;  // lanes 0 .. r-1 published
+                const int e = endm ? __ffs(endm) - 1 : 32;                // first inclusive / skipped / start
+                if (r == 0) {
+                    int quit = 0;
+                    if (lane == 0) {
+                        if (ld_volatile_shared(&ctrl->abort)) quit = 1;
+                        else if ((it & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+                            st_volatile_shared(&ctrl->abort, 1);
+                            atomicOr(&p.hdr->status, ART_STATUS_TIMEOUT);
+                            record_check(p.hdr, 252, item, kk, k);
+                            quit = 1;
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, quit, 0)) return false;
+                    __nanosleep(64);
+                    continue;
+                }
+                const int take = e < r ? e + 1 : r;
+                if (e < take && __shfl_sync(0xffffffffu, fl, e) == 3) {
+                    dead = true;  // a unit before this one was skipped: the item stopped before it
+                    break;
+                }
+                for (int t = 0; t < take; t += 4) {
+                    float M2[4], L2[4], O2[4][SPL];
+                    int ft[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int tq = t + q;
+                        const int ut = kk - tq;
+                        const int f = __shfl_sync(0xffffffffu, fl, tq & 31);
+                        ft[q] = (tq < take && ut >= 0) ? f : 0;
+                        // every lane orders its payload loads after its own acquire of the flag
+                        if (ft[q]) (void)ld_acquire_gpu(&up.tflag[ibase + ut]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int ut = max(kk - (t + q), 0);
+                        const float* src = (ft[q] == 2 ? up.incl : up.agg) + (ibase + ut) * UW;
+                        M2[q] = ft[q] ? __ldcg(src + lane) : -INFINITY;
+                        L2[q] = ft[q] ? __ldcg(src + 32 + lane) : 0.f;
+#pragma unroll
+                        for (int j = 0; j < SPL; ++j) O2[q][j] = ft[q] ? __ldcg(src + (2 + j) * 32 + lane) : 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) merge(cM, cL, cO, M2[q], L2[q], O2[q]);
+                }
+                if (e < take) break;  // reached an inclusive state or the list's start
+                kk -= take;
+            }
+        }
+        int* uf = up.uflags + 4 * iu;
+        if (dead) {
+            if (lane == 0) {
+                st_release_gpu(&up.tflag[iu], 3);
+                st_release_gpu(uf + 2, 3);
+            }
+        } else {
+            {
+                float iM = cM, iL = cL, iO[SPL];
+#pragma unroll
+                for (int j = 0; j < SPL; ++j) iO[j] = cO[j];
+                merge(iM, iL, iO, Ma, La, Oa);
+                float* gi = up.incl + iu * UW;
+                gi[lane] = iM;
+                gi[32 + lane] = iL;
+#pragma unroll
+                for (int j = 0; j < SPL; ++j) gi[(2 + j) * 32 + lane] = iO[j];
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(&up.tflag[iu], 2);
+            }
+            // the stability test of each block of the unit, in list order, from that state
+            float M = cM, Lsum = cL, X[SPL];
+            const float rL = cL > 0.f ? 1.f / cL : 0.f;
+            float q = 0.f;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) {
+                X[j] = hs[j] >= 0 ? cO[j] * rL : 0.f;
+                q = fmaf(X[j], X[j], q);
+            }
+            q = warp_sum(q);
+            const float n0 = sqrtf(q);  // |x| before the unit's first block
+            // pass 1, lane-local: the probe's change over each block (the update of x is
+            // per slot), and this lane's terms of sum delta^2, sum delta . x_{i-1}, |x_i|^2
+            float v[4 * kUnitBlocks];
+#pragma unroll
+            for (int j = 0; j < kUnitBlocks; ++j) {
+                float s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                if (j < nj) {
+                    const float* s = ust + (size_t)j * W * 32;
+                    const float mbk = s[lane], lb = s[32 + lane];
+                    const float Mn = fmaxf(M, mbk);
+                    const float a = exp2f(M - Mn);
+                    const float bw = exp2f(mbk - Mn);
+                    const float Ln = fmaf(a, Lsum, bw * lb);
+                    const float cf = __fdividef(bw, Ln);
+                    M = Mn;
+                    Lsum = Ln;
+#pragma unroll
+                    for (int jj = 0; jj < SPL; ++jj) {
+                        const float pb = s[(2 + jj) * 32 + lane];
+                        const float d = hs[jj] >= 0 ? cf * (pb - lb * X[jj]) : 0.f;
+                        s1 = fmaf(d, d, s1);
+                        s2 = fmaf(d, X[jj], s2);
+                        X[jj] += d;
+                        s3 = fmaf(X[jj], X[jj], s3);
+                    }
+                }
+                v[j] = s1;
+                v[kUnitBlocks + j] = s2;
+                v[2 * kUnitBlocks + j] = s3;
+                v[3 * kUnitBlocks + j] = 0.f;
+            }
+            // pass 2: the warp sums of all of them at once; lane l then holds the sums of
+            // entries 2 l and 2 l + 1
+            transpose_reduce<4 * kUnitBlocks, 32>(v, lane);
+            auto sum_at = [&](int entry) -> float {  // warp sum of entry `entry`, in every lane
+                const float a0 = __shfl_sync(0xffffffffu, v[0], (entry >> 1) & 31);
+                const float a1 = __shfl_sync(0xffffffffu, v[1], (entry >> 1) & 31);
+                return (entry & 1) ? a1 : a0;
+            };
+            // pass 3: lane b takes the test of block b, the same tests as the one-CTA
+            // statistics warp, multiplied through by their positive denominators
+            const int bj = lane < kUnitBlocks ? lane : 0;
+            const float s1 = sum_at(bj), s2 = sum_at(kUnitBlocks + bj), s3 = sum_at(2 * kUnitBlocks + bj);
+            const float s3p = sum_at(2 * kUnitBlocks + (bj > 0 ? bj - 1 : 0));
+            const float nprev = bj == 0 ? n0 : sqrtf(s3p);
+            const float rprev = bj == 0 ? (n0 > 0.f ? 1.f / n0 : 0.f) : __fdividef(1.f, nprev);
+            const float ni = sqrtf(s3);
+            const float S = ni + nprev, T = 2.f * s2 + s1;
+            const bool mag_ok = fabsf(T) * rprev < p.eps_mag * S;
+            const float Nd = fmaf(s1, S * S, fmaf(-2.f * s2 * T, S * rprev, T * T));
+            const bool dir_ok = fmaxf(0.f, Nd) < 2.f * p.eps_dir * s3 * (S * S);
+            const int pos = k * up.ck + bj;
+            const bool stable = lane < nj && pos >= 1 && nprev > 0.f && ni > 0.f && nprev < 1e30f && ni < 1e30f &&
+                                mag_ok && dir_ok;
+            const uint32_t bits = __ballot_sync(0xffffffffu, stable);
+            if (lane == 0) {
+                uf[0] = (int)bits;
+                uf[1] = nj;
+                st_release_gpu(uf + 2, 1);
+            }
+            // the patience count entering the unit: the previous unit's trailing stable run
+            int counter = 0;
+            bool dead2 = false;
+            if (k > 0) {
+                const int* pf = up.uflags + 4 * (iu - 1);
+                int st = 0;
+                if (!poll_flag(pf + 2, 1, st, ctrl, p.hdr, 253)) return false;
+                if (st == 3) {
+                    dead2 = true;
+                } else {
+                    const uint32_t pbits = (uint32_t)__ldcg(pf);
+                    const int pn = __ldcg(pf + 1);
+                    int run = 0;
+                    for (int jj = pn - 1; jj >= 0 && ((pbits >> jj) & 1u); --jj) ++run;
+                    counter = min(run, p.patience);
+                }
+            }
+            if (!dead2) {
+                const ItemInfo inf = p.info[item];
+                const int n = inf.n;
+                const bool has0 = (inf.flags & kItemHas0) != 0;
+                const int pz = up.p0[item];
+                int cand = -1;
+                for (int j = 0; j < nj; ++j) {
+                    const int pos = k * up.ck + j;
+                    const bool st = (bits >> j) & 1u;
+                    counter = st ? min(counter + 1, p.patience) : 0;
+                    const bool seen0 = !has0 || pos >= pz;
+                    if (pos == n - 1 || (st && counter >= p.patience && seen0)) {
+                        cand = pos;
+                        break;
+                    }
+                }
+                if (cand >= 0 && lane == 0) atomicMin(&up.stop_min[item], cand);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) red_release_add(&up.resolved[item], 1);  // after this lane's atomicMin and flags
+        return true;
+    };
+
+    for (int rec = 0;; ++rec) {
+        const int rb = rec % NB;
+        if (!wait_bounded(&part_full[rb], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 251)) return;
+        const URec ri = rinfo[rb];
+        if (ri.kind != kUBlock) return;
+        if (ri.j < 0 || ri.j >= ri.nj || ri.nj > up.ck || ri.item < 0 || ri.item >= p.num_items || ri.k < 0 ||
+            ri.k >= up.maxk) {
+            if (lane == 0) record_check(p.hdr, 254, ri.item, ri.k, ri.j);
+            return;
+        }
+        // block max and weight sum of this lane's head over the 4 warps (each used its own max),
+        // and the block's probe sums at that max
+        float sw[RGW];
+        float mbk = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < RGW; ++w) {
+            sw[w] = pmb[(rb * RGW + w) * G + hme];
+            mbk = fmaxf(mbk, sw[w]);
+        }
+        float lb = 0.f;
+#pragma unroll
+        for (int w = 0; w < RGW; ++w) {
+            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a warp without valid keys adds nothing
+            lb = fmaf(sw[w], plb[(rb * RGW + w) * G + hme], lb);
+        }
+        const float* pp = part + (size_t)rb * NPR * C::PST;
+        float pb[SPL];
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < RGW; ++w) {
+                float pw = 0.f;
+#pragma unroll
+                for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
+                v = fmaf(sw[w], pw, v);
+            }
+            pb[j] = hs[j] >= 0 ? v : 0.f;  // slots past the probe hold no data
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, &part_empty[rb]);
+        float* s = ust + (size_t)ri.j * W * 32;
+        s[lane] = mbk;
+        s[32 + lane] = lb;
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) s[(2 + j) * 32 + lane] = pb[j];
+        if (ri.j == 0) {
+            Ma = mbk;
+            La = lb;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) Oa[j] = pb[j];
+        } else {
+            merge(Ma, La, Oa, mbk, lb, pb);
+        }
+        if (ri.j == ri.nj - 1) {
+            __syncwarp();
+            if (!finish_unit(ri.item, ri.k, ri.nj)) return;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the kernels
+// ---------------------------------------------------------------------------
+template <int D, int G>
+__global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
+    art_units_kernel(const Params p, const UParams up0, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv) {
+    UParams up = up0;
+    up.ck = p.hdr->ck;  // chosen by the plan kernel
+    using C = typename UCfg<D, G>::C;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const ULayout L = make_ulayout<D, G>(p.stages);
+    unsigned char* ring = smem;
+    UMeta* meta = reinterpret_cast<UMeta*>(smem + L.meta);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* empty = full + p.stages;
+    uint64_t* part_full = empty + p.stages;
+    uint64_t* part_empty = part_full + C::NB;
+    int* prank = reinterpret_cast<int*>(smem + L.ptab);
+    URec* rinfo = reinterpret_cast<URec*>(smem + L.rinfo);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::GW);
+        }
+        for (int b = 0; b < C::NB; ++b) {
+            mbar_init(&part_full[b], C::GW);
+            mbar_init(&part_empty[b], 1);
+        }
+        ctrl->stop_item = -1;
+        ctrl->abort = 0;
+        fence_mbar_init();
+    }
+    if (tid < D) {
+        // rank of head dim `tid` among the probe dims, or -1
+        int found = 0, rank = 0;
+        for (int k = 0; k < p.m; ++k) {
+            const int col = p.probe[k];
+            if (col == tid) found = 1;
+            if (col >= 0 && col < tid) ++rank;
+        }
+        prank[tid] = found ? rank : -1;
+    }
+    if (tid == 4 * 32) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+    }
+    __syncthreads();
+    const int warp = tid >> 5;
+    if (warp == 4) {
+        producer_u<C>(p, up, ring, meta, full, empty, ctrl, &tk, &tv);
+    } else if (warp == 5) {
+        stat_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
+                  reinterpret_cast<const float*>(smem + L.pmb), part_full, part_empty, rinfo,
+                  reinterpret_cast<float*>(smem + L.ust), ctrl);
+    } else {
+        consumer_u<C>(p, up, ring, meta, full, empty, part_full, part_empty, rinfo, L, smem, prank, ctrl);
+    }
+}
+
+// Per (item, query head): merge the partials of the units before the stopping unit
+// and of the fix pieces (or of the stopping unit itself when it ends at the stop),
+// write O = sums / weight sums and blocks_used. Warp w takes partials w, w + 8, ...,
+// 32 at a time: lane i loads the max and weight sum of the i-th, then the warp adds
+// the 32 partials' sums with their loads in flight together; lane l holds head dims
+// l, l + 32, ...
+template <int D, int G>
+__global__ void __launch_bounds__(256) art_units_combine(const Params p, const UParams up0) {
+    using E = Elem<true>;
+    // launched while the unit kernel may still run: wait for it to finish
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    UParams up = up0;
+    up.ck = p.hdr->ck;
+    constexpr int ND = D / 32;
+    __shared__ float s_m[8], s_l[8], s_o[8][D];
+    const int item = blockIdx.x, h = blockIdx.y;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
+    const size_t obase = ((size_t)b * p.Hq + (size_t)g * G + h) * D;
+    const ItemInfo inf = p.info[item];
+    const bool bad = (inf.flags & kItemBad) || up.fail[item] != 0;
+    const int n = bad ? 0 : inf.n;
+    const int t = n > 0 ? up.stop_min[item] : -1;
+    if (bad || n == 0 || t < 0 || t >= n) {
+        if (!bad && n > 0 && threadIdx.x == 0 && h == 0) record_check(p.hdr, 261, item, t, n);
+        for (int d = threadIdx.x; d < D; d += blockDim.x) E::store(p.out, obase + d, 0.f);
+        if (threadIdx.x == 0 && h == 0) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
+        return;
+    }
+    if (threadIdx.x == 0 && h == 0) p.blocks_used[item] = t + 1;
+    const int kk = t / up.ck, sfirst = kk * up.ck;
+    const bool use_fix = t != min(n, sfirst + up.ck) - 1;
+    const int nunits = use_fix ? kk : kk + 1;        // whole units
+    const int npieces = use_fix ? t - sfirst + 1 : 0;  // fix pieces (one block each)
+    const int nq = (nunits + npieces) * 4;             // partials, 4 warps each
+    auto base_of = [&](int qi, const float*& po, const float*& pml) {
+        const int ui = qi >> 2;
+        size_t x;
+        if (ui < nunits) {
+            x = (size_t)item * up.maxk + ui;
+            po = up.part_o + x * 32 * D;
+            pml = up.part_ml + x * 64;
+        } else {
+            x = (size_t)item * up.ck + (ui - nunits);
+            po = up.fix_o + x * 32 * D;
+            pml = up.fix_ml + x * 64;
+        }
+    };
+    // fragment position of (h, d): lane 4 (d % 8) + h / 2, word 4 (d / 16) + 2 ((d / 8) % 2) + h % 2
+    int off[ND];
+#pragma unroll
+    for (int i = 0; i < ND; ++i) {
+        const int d = lane + 32 * i;
+        off[i] = (4 * (d & 7) + (h >> 1)) * (D / 4) + 4 * (d >> 4) + 2 * ((d >> 3) & 1) + (h & 1);
+    }
+    float M = -INFINITY, Lw = 0.f, O[ND];
+#pragma unroll
+    for (int i = 0; i < ND; ++i) O[i] = 0.f;
+    for (int q0 = w; q0 < nq; q0 += 8 * 32) {
+        const int qi = q0 + 8 * lane;
+        float mi = -INFINITY, li = 0.f;
+        if (qi < nq) {
+            const float* po;
+            const float* pml;
+            base_of(qi, po, pml);
+            mi = pml[(qi & 3) * 16 + h];
+            li = pml[(qi & 3) * 16 + 8 + h];
+        }
+        float mx = mi;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (mx == -INFINITY) continue;  // no partial here saw a valid key
+        const float Mn = fmaxf(M, mx);
+        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        const float fi = mi == -INFINITY ? 0.f : exp2f(mi - Mn);
+        Lw = fmaf(a, Lw, warp_sum(fi * li));
+#pragma unroll
+        for (int i = 0; i < ND; ++i) O[i] *= a;
+        M = Mn;
+        const int cnt = min(32, (nq - q0 + 7) / 8);
+#pragma unroll 4
+        for (int x = 0; x < cnt; ++x) {
+            const float f = __shfl_sync(0xffffffffu, fi, x);
+            const int q = q0 + 8 * x;
+            const float* po;
+            const float* pml;
+            base_of(q, po, pml);
+            const float* src = po + (size_t)(q & 3) * 32 * (D / 4);
+#pragma unroll
+            for (int i = 0; i < ND; ++i) O[i] = fmaf(f, src[off[i]], O[i]);
+        }
+    }
+    if (lane == 0) {
+        s_m[w] = M;
+        s_l[w] = Lw;
+    }
+#pragma unroll
+    for (int i = 0; i < ND; ++i) s_o[w][lane + 32 * i] = O[i];
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) mx = fmaxf(mx, s_m[x]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const float f = s_m[x] == -INFINITY ? 0.f : exp2f(s_m[x] - mx);
+            num = fmaf(f, s_o[x][d], num);
+            den = fmaf(f, s_l[x], den);
+        }
+        E::store(p.out, obase + d, num / den);
+    }
+}
+
+// Largest ring depth (2..8 slots) that lets `want` CTAs share one SM.
+template <int D, int G>
+inline int pick_ustages(int want, int smem_per_sm, int smem_per_block) {
+    for (int s = 8; s >= 2; --s) {
+        const size_t t = make_ulayout<D, G>(s).total;
+        if ((int)t <= smem_per_block && (size_t)want * (t + 1024) <= (size_t)smem_per_sm) return s;
+    }
+    return 0;
+}
+
+template <int D, int G>
+cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* li) {
+    auto kern = art_units_kernel<D, G>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int sms = 0, smem_sm = 0, smem_blk = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    const char* envs = std::getenv("ART_STAGES");
+    const int force = envs ? std::atoi(envs) : 0;
+    int stages = force >= 2 && force <= 8 ? force : pick_ustages<D, G>(2, smem_sm, smem_blk);
+    if (stages == 0) stages = pick_ustages<D, G>(1, smem_sm, smem_blk);
+    if (stages == 0) return cudaErrorInvalidConfiguration;
+    const size_t smem = make_ulayout<D, G>(stages).total;
+    if ((int)smem > smem_blk) return cudaErrorInvalidConfiguration;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    int occ = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, UCfg<D, G>::THREADS, smem)) != cudaSuccess)
+        return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    const long long rows = (long long)p.num_pages * p.Hkv * p.Ps;
+    if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
+    const char* env3 = std::getenv("ART_TMA3D");
+    p.tma3d = (!env3 || std::atoi(env3) != 0) && make_cache_map3(&tk, p.k, rows, D, p.Ps) == cudaSuccess &&
+              make_cache_map3(&tv, p.v, rows, D, p.Ps) == cudaSuccess;
+    if (!p.tma3d) {
+        if ((e = make_cache_map(&tk, p.k, rows, D, p.Ps)) != cudaSuccess) return e;
+        if ((e = make_cache_map(&tv, p.v, rows, D, p.Ps)) != cudaSuccess) return e;
+    }
+    p.stages = stages;
+    const int grid = sms * occ;
+    if (li) {
+        li->grid = grid;
+        li->stages = stages;
+        li->smem = smem;
+        li->ctas_per_sm = occ;
+    }
+    kern<<<grid, UCfg<D, G>::THREADS, smem, stream>>>(p, up, tk, tv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the merge kernel may start while the unit kernel drains (programmatic dependent
+    // launch); it waits for the unit kernel's completion before reading anything
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(p.num_items, G);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, art_units_combine<D, G>, p, up);
+}
+
+}  // namespace art
+
+#define ART_UNITS_INSTANTIATE(D, G) \
+    template cudaError_t art::launch_units<D, G>(art::Params, art::UParams, cudaStream_t, art::LaunchInfo*);

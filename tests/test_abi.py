@@ -102,8 +102,16 @@ def test_dense_host_checks(lib):
 
 
 def test_workspace_size(lib):
-    s = good_shape(batch=3, num_kv_heads=4, num_q_heads=16)
+    # one CTA per item: the 64-byte header, then per item {n, flags} and a claim-order slot
+    s = good_shape(batch=3, num_kv_heads=4, num_q_heads=16, dtype=1)
     assert K.art_workspace_bytes(s) == 64 + 12 * 12
+    big = good_shape(batch=300, num_kv_heads=1, num_q_heads=1)  # bf16, more items than the unit path takes
+    assert K.art_workspace_bytes(big) == 64 + 12 * 300
+    # bf16 with few items: plus the unit path's area, which grows with the longest possible list
+    small = good_shape(batch=3, num_kv_heads=4, num_q_heads=16)
+    longer = good_shape(batch=3, num_kv_heads=4, num_q_heads=16, max_pages_per_seq=8 * 64)
+    assert K.art_workspace_bytes(small) > 64 + 12 * 12
+    assert K.art_workspace_bytes(longer) > K.art_workspace_bytes(small)
     assert lib.art_workspace_bytes(None) == 0
 
 
