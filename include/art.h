@@ -116,8 +116,9 @@ size_t art_workspace_bytes(const art_shape* shape);
  * (an addition of this library; the ART paper describes one CTA per sequence):
  *   0  one CTA per item (b, g): a persistent kernel whose CTAs claim whole
  *      items, longest lists first;
- *   1  the unit path: each item's list is cut into units of 16 blocks that
- *      any CTA may take, so one item is spread over many SMs; the stop is
+ *   1  the unit path: each item's list is cut into units of 8 to 16 blocks
+ *      (chosen per call so that the units fill whole waves of CTAs) that any
+ *      CTA may take, so one item is spread over many SMs; the stop is
  *      found from per-unit statistics joined by a look-back, the blocks of
  *      the stopping unit up to the stop are recomputed, and a second kernel
  *      merges the units' partial outputs. Blocks of units claimed before the

@@ -53,6 +53,7 @@ namespace art {
 
 constexpr int kUnitBlocks = 16;     // ck: ART blocks per unit at most
 constexpr int kUnitMinBlocks = 8;   // ... and at least (the workspace is sized for it)
+constexpr int kUnitRecs = 4;        // block records in flight from the consumers to the statistics warp
 constexpr int kUnitMaxItems = 256;  // the unit path is offered up to this many items
 constexpr int kUnitMaxK = 4096;     // units per item at most
 constexpr int kUnitWords = 10;      // words per lane of a probe state: max, weight sum, 8 probe slots
@@ -66,6 +67,8 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
     asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// orders this thread's earlier memory accesses before its later ones, GPU scope
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // atomic add with release semantics: this thread's earlier writes are visible first
 __device__ __forceinline__ void red_release_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -151,14 +154,14 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)stages * sizeof(UMeta);
     o = align_up(o, 16);
     L.bars = o;  // full[stages], empty[stages], part_full[NB], part_empty[NB]
-    o += (size_t)(2 * stages + 2 * C::NB) * sizeof(uint64_t);
+    o += (size_t)(2 * stages + 2 * kUnitRecs) * sizeof(uint64_t);
     o = align_up(o, 16);
     L.part = o;  // [NB][4 warps][PRW][PST] probe partial rows
-    o += (size_t)C::NB * C::GW * C::PRW * C::PST * sizeof(float);
+    o += (size_t)kUnitRecs * C::GW * C::PRW * C::PST * sizeof(float);
     L.plb = o;  // [NB][4][G] block weight sums
-    o += (size_t)C::NB * C::GW * G * sizeof(float);
+    o += (size_t)kUnitRecs * C::GW * G * sizeof(float);
     L.pmb = o;  // [NB][4][G] block maxima
-    o += (size_t)C::NB * C::GW * G * sizeof(float);
+    o += (size_t)kUnitRecs * C::GW * G * sizeof(float);
     o = align_up(o, 1024);
     L.qt = o;  // the unit's queries, 8 rows (heads past G zero), 128B-swizzled
     o += (size_t)8 * C::ROWB;
@@ -166,7 +169,7 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)D * sizeof(int);
     o = align_up(o, 16);
     L.rinfo = o;
-    o += (size_t)C::NB * sizeof(URec);
+    o += (size_t)kUnitRecs * sizeof(URec);
     o = align_up(o, 16);
     L.ust = o;  // [ck][W][32 lanes] block summaries of the unit being tested
     o += (size_t)kUnitBlocks * UCfg<D, G>::W * 32 * sizeof(float);
@@ -432,7 +435,7 @@ template <class C>
 __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ring, const UMeta* meta,
                            uint64_t* full, uint64_t* empty, uint64_t* part_full, uint64_t* part_empty, URec* rinfo,
                            const ULayout& L, unsigned char* smem, const int* prank, Ctrl* ctrl) {
-    constexpr int G = C::GQ, D = C::DD, KS = C::KS, GW = C::GW, NB = C::NB;
+    constexpr int G = C::GQ, D = C::DD, KS = C::KS, GW = C::GW, NB = kUnitRecs;
     constexpr bool SPLITN = C::SPLITN;
     const int wg = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane >> 2, tig = lane & 3;
@@ -729,7 +732,7 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
 template <class C>
 __device__ void stat_u(const Params& p, const UParams& up, const float* part, const float* plb, const float* pmb,
                        uint64_t* part_full, uint64_t* part_empty, const URec* rinfo, float* ust, Ctrl* ctrl) {
-    constexpr int G = C::GQ, SPL = C::SPL, NB = C::NB, RGW = C::RGW;
+    constexpr int G = C::GQ, SPL = C::SPL, NB = kUnitRecs, RGW = C::RGW;
     constexpr int NPR = C::RGW * C::PRW;  // partial rows per record
     constexpr int W = SPL + 2;
     constexpr int UW = 32 * kUnitWords;   // floats of one probe state in the workspace
@@ -768,7 +771,7 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
             ga[32 + lane] = La;
 #pragma unroll
             for (int j = 0; j < SPL; ++j) ga[(2 + j) * 32 + lane] = Oa[j];
-            __threadfence();
+            fence_acq_rel_gpu();
             __syncwarp();
             if (lane == 0) st_release_gpu(&up.tflag[iu], 1);
         }
@@ -852,14 +855,12 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
 #pragma unroll
                 for (int j = 0; j < SPL; ++j) iO[j] = cO[j];
                 merge(iM, iL, iO, Ma, La, Oa);
+                // its flag follows after the tests' first pass, when these stores are done
                 float* gi = up.incl + iu * UW;
                 gi[lane] = iM;
                 gi[32 + lane] = iL;
 #pragma unroll
                 for (int j = 0; j < SPL; ++j) gi[(2 + j) * 32 + lane] = iO[j];
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(&up.tflag[iu], 2);
             }
             // the stability test of each block of the unit, in list order, from that state
             float M = cM, Lsum = cL, X[SPL];
@@ -903,6 +904,9 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
                 v[2 * kUnitBlocks + j] = s3;
                 v[3 * kUnitBlocks + j] = 0.f;
             }
+            fence_acq_rel_gpu();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(&up.tflag[iu], 2);  // the inclusive state
             // pass 2: the warp sums of all of them at once; lane l then holds the sums of
             // entries 2 l and 2 l + 1
             transpose_reduce<4 * kUnitBlocks, 32>(v, lane);
@@ -1052,7 +1056,7 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + p.stages;
     uint64_t* part_full = empty + p.stages;
-    uint64_t* part_empty = part_full + C::NB;
+    uint64_t* part_empty = part_full + kUnitRecs;
     int* prank = reinterpret_cast<int*>(smem + L.ptab);
     URec* rinfo = reinterpret_cast<URec*>(smem + L.rinfo);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
@@ -1062,7 +1066,7 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C::GW);
         }
-        for (int b = 0; b < C::NB; ++b) {
+        for (int b = 0; b < kUnitRecs; ++b) {
             mbar_init(&part_full[b], C::GW);
             mbar_init(&part_empty[b], 1);
         }
@@ -1097,12 +1101,12 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     }
 }
 
-// Per (item, query head): merge the partials of the units before the stopping unit
-// and of the fix pieces (or of the stopping unit itself when it ends at the stop),
-// write O = sums / weight sums and blocks_used. Warp w takes partials w, w + 8, ...,
-// 32 at a time: lane i loads the max and weight sum of the i-th, then the warp adds
-// the 32 partials' sums with their loads in flight together; lane l holds head dims
-// l, l + 32, ...
+// Per (item, query head, 32 head dims): merge the partials of the units before the
+// stopping unit and of the fix pieces (or of the stopping unit itself when it ends at
+// the stop), write O = sums / weight sums and blocks_used. Lane l holds head dim
+// 32 blockIdx.z + l; warp w takes partials w, w + 8, ..., 32 at a time: lane i loads
+// the max and weight sum of the i-th, then the warp adds their sums with all the loads
+// in flight together.
 template <int D, int G>
 __global__ void __launch_bounds__(256) art_units_combine(const Params p, const UParams up0) {
     using E = Elem<true>;
@@ -1110,10 +1114,11 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
     asm volatile("griddepcontrol.wait;" ::: "memory");
     UParams up = up0;
     up.ck = p.hdr->ck;
-    constexpr int ND = D / 32;
-    __shared__ float s_m[8], s_l[8], s_o[8][D];
+    __shared__ float s_m[8], s_l[8], s_o[8][32];
     const int item = blockIdx.x, h = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = 32 * blockIdx.z + lane;
+    const bool lead = threadIdx.x == 0 && h == 0 && blockIdx.z == 0;
     const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
     const size_t obase = ((size_t)b * p.Hq + (size_t)g * G + h) * D;
     const ItemInfo inf = p.info[item];
@@ -1121,18 +1126,20 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
     const int n = bad ? 0 : inf.n;
     const int t = n > 0 ? up.stop_min[item] : -1;
     if (bad || n == 0 || t < 0 || t >= n) {
-        if (!bad && n > 0 && threadIdx.x == 0 && h == 0) record_check(p.hdr, 261, item, t, n);
-        for (int d = threadIdx.x; d < D; d += blockDim.x) E::store(p.out, obase + d, 0.f);
-        if (threadIdx.x == 0 && h == 0) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
+        if (!bad && n > 0 && lead) record_check(p.hdr, 261, item, t, n);
+        if (w == 0) E::store(p.out, obase + d, 0.f);
+        if (lead) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
         return;
     }
-    if (threadIdx.x == 0 && h == 0) p.blocks_used[item] = t + 1;
+    if (lead) p.blocks_used[item] = t + 1;
     const int kk = t / up.ck, sfirst = kk * up.ck;
     const bool use_fix = t != min(n, sfirst + up.ck) - 1;
     const int nunits = use_fix ? kk : kk + 1;        // whole units
     const int npieces = use_fix ? t - sfirst + 1 : 0;  // fix pieces (one block each)
     const int nq = (nunits + npieces) * 4;             // partials, 4 warps each
-    auto base_of = [&](int qi, const float*& po, const float*& pml) {
+    // fragment position of (h, d): lane 4 (d % 8) + h / 2, word 4 (d / 16) + 2 ((d / 8) % 2) + h % 2
+    const int off = (4 * (d & 7) + (h >> 1)) * (D / 4) + 4 * (d >> 4) + 2 * ((d >> 3) & 1) + (h & 1);
+    auto part_of = [&](int qi, const float*& po, const float*& pml) {
         const int ui = qi >> 2;
         size_t x;
         if (ui < nunits) {
@@ -1144,26 +1151,19 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
             po = up.fix_o + x * 32 * D;
             pml = up.fix_ml + x * 64;
         }
+        po += (size_t)(qi & 3) * 32 * (D / 4);
+        pml += (qi & 3) * 16;
     };
-    // fragment position of (h, d): lane 4 (d % 8) + h / 2, word 4 (d / 16) + 2 ((d / 8) % 2) + h % 2
-    int off[ND];
-#pragma unroll
-    for (int i = 0; i < ND; ++i) {
-        const int d = lane + 32 * i;
-        off[i] = (4 * (d & 7) + (h >> 1)) * (D / 4) + 4 * (d >> 4) + 2 * ((d >> 3) & 1) + (h & 1);
-    }
-    float M = -INFINITY, Lw = 0.f, O[ND];
-#pragma unroll
-    for (int i = 0; i < ND; ++i) O[i] = 0.f;
+    float M = -INFINITY, Lw = 0.f, O = 0.f;
     for (int q0 = w; q0 < nq; q0 += 8 * 32) {
         const int qi = q0 + 8 * lane;
         float mi = -INFINITY, li = 0.f;
         if (qi < nq) {
             const float* po;
             const float* pml;
-            base_of(qi, po, pml);
-            mi = pml[(qi & 3) * 16 + h];
-            li = pml[(qi & 3) * 16 + 8 + h];
+            part_of(qi, po, pml);
+            mi = pml[h];
+            li = pml[8 + h];
         }
         float mx = mi;
 #pragma unroll
@@ -1173,30 +1173,30 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
         const float a = M == -INFINITY ? 0.f : exp2f(M - Mn);
         const float fi = mi == -INFINITY ? 0.f : exp2f(mi - Mn);
         Lw = fmaf(a, Lw, warp_sum(fi * li));
-#pragma unroll
-        for (int i = 0; i < ND; ++i) O[i] *= a;
+        O *= a;
         M = Mn;
         const int cnt = min(32, (nq - q0 + 7) / 8);
-#pragma unroll 4
-        for (int x = 0; x < cnt; ++x) {
-            const float f = __shfl_sync(0xffffffffu, fi, x);
-            const int q = q0 + 8 * x;
-            const float* po;
-            const float* pml;
-            base_of(q, po, pml);
-            const float* src = po + (size_t)(q & 3) * 32 * (D / 4);
+        float v[32];
 #pragma unroll
-            for (int i = 0; i < ND; ++i) O[i] = fmaf(f, src[off[i]], O[i]);
+        for (int x = 0; x < 32; ++x) {
+            v[x] = 0.f;
+            if (x < cnt) {
+                const float* po;
+                const float* pml;
+                part_of(q0 + 8 * x, po, pml);
+                v[x] = po[off];
+            }
         }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) O = fmaf(__shfl_sync(0xffffffffu, fi, x), v[x], O);
     }
     if (lane == 0) {
         s_m[w] = M;
         s_l[w] = Lw;
     }
-#pragma unroll
-    for (int i = 0; i < ND; ++i) s_o[w][lane + 32 * i] = O[i];
+    s_o[w][lane] = O;
     __syncthreads();
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    if (w == 0) {
         float mx = -INFINITY;
 #pragma unroll
         for (int x = 0; x < 8; ++x) mx = fmaxf(mx, s_m[x]);
@@ -1204,7 +1204,7 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
             const float f = s_m[x] == -INFINITY ? 0.f : exp2f(s_m[x] - mx);
-            num = fmaf(f, s_o[x][d], num);
+            num = fmaf(f, s_o[x][lane], num);
             den = fmaf(f, s_l[x], den);
         }
         E::store(p.out, obase + d, num / den);
@@ -1272,7 +1272,7 @@ cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* 
     // launch); it waits for the unit kernel's completion before reading anything
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(p.num_items, G);
+    cfg.gridDim = dim3(p.num_items, G, D / 32);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

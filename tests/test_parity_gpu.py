@@ -143,8 +143,8 @@ def test_shapes(spec):
 
 @pytest.mark.parametrize("p", [1, 2, 4, 16, 17])
 def test_long_lists(p):
-    """Lists of 141 and 235 blocks (9 and 15 units of 16 blocks on the unit
-    path), stops anywhere in a unit, patience up to the unit length and past it
+    """Lists of 141 and 235 blocks (9 to 30 units of 8 to 16 blocks on the unit
+    path), stops anywhere in a unit, patience up to the longest unit and past it
     (where the unit path is not taken)."""
     w = W.build("long", seed=51, dtype="bf16", batch=2, num_q_heads=14, num_kv_heads=2, head_dim=128,
                 page_size=16, block_size=64, seq_lens=[15000, 9000], paged="permuted", plant=True,
