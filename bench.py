@@ -186,17 +186,18 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def load_traffic(config_name, alg_bytes):
-    """DRAM bytes (read + write) per decode-kernel launch from the committed ncu
-    summary of this workload, only if it was taken on the current kernel
-    source. A capture of a smaller batch of the same workload is scaled by the
-    algorithmic bytes of the two launches."""
+def load_traffic(config_name, alg_bytes, path):
+    """DRAM bytes (read + write) per decode call from the committed ncu summary
+    of this workload, only if it was taken on the current kernel source and the
+    same kernel path ("units" or "one CTA per item"). A capture of a smaller
+    batch of the same workload is scaled by the algorithmic bytes of the two
+    launches."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None, None
     d = json.load(open(p))
     e = d.get(config_name)
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or e.get("kernel_hash") != kernel_source_hash() or e.get("path") != path:
         return None, None
     t = float(e["dram_bytes"]) * alg_bytes / float(e["algorithmic_bytes"])
     src = f"ncu capture of {e['captured_workload']}" + \
@@ -352,6 +353,8 @@ def run_ours(args):
         t_d, t_dk = time_calls(dense_call, args.steps, kernel=True)
         ms_d, ms_dk = float(t_d.mean()), float(t_dk.mean())
         dense = {"queries_per_s": queries / (ms_d * 1e-3), "ms_per_step": ms_d, "kernel_ms": ms_dk,
+                 "path": "units" if K.art_decode_path(dev.shape, 1, dev.workspace.numel()) == 1
+                 else "one CTA per item",
                  "kernel_gbs": (kv_bytes(w) + side_bytes(w)) / (ms_dk * 1e-3) / 1e9,
                  "speedup_art_over_dense": ms_d / ms}
         # the detector's own cost: ART with eps = 0 never stops
@@ -368,7 +371,7 @@ def run_ours(args):
     peak, peak_kind = load_peaks()
     alg = kv_bytes(w, bu) + side_bytes(w)
     achieved = alg / (ms_kernel * 1e-3) / 1e9
-    traffic, traffic_src = load_traffic(w.name, alg)
+    traffic, traffic_src = load_traffic(w.name, alg, "units" if path == 1 else "one CTA per item")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "traffic_source": traffic_src, "peak_kind": peak_kind,
                 "kernel": kernels, "path": "units" if path == 1 else "one CTA per item",

@@ -126,7 +126,9 @@ size_t art_workspace_bytes(const art_shape* shape);
  * The unit path is taken for bf16 when batch * num_kv_heads is at most 256 and
  * below the number of SMs / 2, patience <= 16 and workspace_bytes covers its
  * area; the environment variable ART_UNITS=0 or 1 forces the choice where the
- * path is offered. A shape that fails the argument checks returns 0.
+ * path is offered. dense_decode takes the same path as art_decode with
+ * patience 1 (there: all units, no statistics, no recompute). A shape that
+ * fails the argument checks returns 0.
  */
 int art_decode_path(const art_shape* shape, int32_t patience, size_t workspace_bytes);
 

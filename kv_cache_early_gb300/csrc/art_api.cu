@@ -27,8 +27,9 @@ struct PlanParams {
     ItemInfo* info;
     int Hkv, Ps, max_pages, max_visit, m, D, num_pages, num_items;
     // unit path (units != 0): its per-item and per-unit state, and the unit list;
-    // ctas = CTAs of the unit kernel (sets the unit length), patience = the call's
-    int units, maxk, ctas, patience;
+    // ctas = CTAs of the unit kernel (sets the unit length), patience = the call's;
+    // dense = the full-scan twin (every item stops at its last block, no fix pieces)
+    int units, maxk, ctas, patience, dense;
     int* p0;
     int* stop_min;
     int* resolved;
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
             acc += t;
         }
         p.hdr->n_regular = acc;
-        p.hdr->n_units = acc + p.num_items * s_ck;  // then ck fix pieces per item
+        p.hdr->n_units = acc + (p.dense ? 0 : p.num_items * s_ck);  // then ck fix pieces per item
     }
     __syncthreads();
     int acc = s_part2[tid];
@@ -251,6 +252,11 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     }
     __syncthreads();
     for (int k = 0; k < my_nch; ++k) p.ulist[s_hist[k] + o] = make_int2(my_item, k);
+    if (p.dense && my_item >= 0 && my_nch > 0) {
+        // the twin reads every listed block: each item stops at its last one
+        p.stop_min[my_item] = __ldcg(reinterpret_cast<const int*>(&p.info[my_item])) - 1;
+        p.resolved[my_item] = my_nch;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -301,14 +307,15 @@ static cudaError_t dispatch(const art_shape& s, const Params& p, cudaStream_t st
     return cudaErrorInvalidValue;
 }
 
-template <int D, int G>
+template <int D, int G, bool kART>
 cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* li);
 
+template <bool kART>
 static cudaError_t dispatch_units(const art_shape& s, const Params& p, const UParams& up, cudaStream_t st,
                                   LaunchInfo* li) {
     const int G = s.num_q_heads / s.num_kv_heads;
 #define ART_UCASE(DD, GG) \
-    if (s.head_dim == DD && G == GG) return launch_units<DD, GG>(p, up, st, li);
+    if (s.head_dim == DD && G == GG) return launch_units<DD, GG, kART>(p, up, st, li);
 #define ART_UCASES(DD) ART_UCASE(DD, 1) ART_UCASE(DD, 2) ART_UCASE(DD, 4) ART_UCASE(DD, 7) ART_UCASE(DD, 8)
     ART_UCASES(128)
     ART_UCASES(64)
@@ -390,7 +397,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     ItemInfo* info = reinterpret_cast<ItemInfo*>(hdr + 1);
     int32_t* order = reinterpret_cast<int32_t*>(info + num_items);
 
-    const bool units = kART && want_units(s, patience, workspace_bytes);
+    const bool units = want_units(s, kART ? patience : 1, workspace_bytes);
     UParams up;
     std::memset(&up, 0, sizeof up);
     if (units) {
@@ -433,7 +440,8 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     pp.num_items = num_items;
     pp.units = units ? 1 : 0;
     pp.maxk = up.maxk;
-    pp.patience = patience;
+    pp.patience = kART ? patience : 1;
+    pp.dense = kART ? 0 : 1;
     pp.ctas = 0;
     if (units) {
         int dev = 0, sms = 0;
@@ -481,7 +489,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     p.ph = probe_heads > 0 ? probe_heads : s.num_q_heads / s.num_kv_heads;
     p.tma3d = 0;
     if (t_events.start && (e = cudaEventRecord(t_events.start, st)) != cudaSuccess) return cuda_fail(e);
-    e = units ? dispatch_units(s, p, up, st, li) : dispatch<kART>(s, p, st, env_stages(), li);
+    e = units ? dispatch_units<kART>(s, p, up, st, li) : dispatch<kART>(s, p, st, env_stages(), li);
     if (e != cudaSuccess) return cuda_fail(e);
     if (t_events.stop && (e = cudaEventRecord(t_events.stop, st)) != cudaSuccess) return cuda_fail(e);
     return ART_OK;

@@ -42,6 +42,10 @@
 // A unit whose item has already stopped before it when it is claimed is
 // skipped; units claimed before the stop was known are read and discarded.
 //
+// The dense twin (kART = false) runs the same units without the statistics:
+// the plan sets every item's stop to its last block, no fix pieces exist, and
+// the merge combines all units.
+//
 // A CTA waits on another CTA's unit only for a unit claimed earlier; every CTA
 // works through its units in claim order and the compute of a unit never
 // waits on another unit, so the waits end. They are bounded all the same.
@@ -431,7 +435,7 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
 // ---------------------------------------------------------------------------
 // consumer warps (one group of 4; warp wg owns keys 16 wg .. 16 wg + 15 of a block)
 // ---------------------------------------------------------------------------
-template <class C>
+template <class C, bool kART>
 __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ring, const UMeta* meta,
                            uint64_t* full, uint64_t* empty, uint64_t* part_full, uint64_t* part_empty, URec* rinfo,
                            const ULayout& L, unsigned char* smem, const int* prank, Ctrl* ctrl) {
@@ -595,7 +599,7 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
             __syncwarp();
             mbar_arrive_if(lane == 0, &empty[slot]);
             UMeta endm = mt;
-            publish(endm, kUEnd, false);
+            if (kART) publish(endm, kUEnd, false);
             return;
         }
         unsigned char* sK = ring + (size_t)slot * C::SLOT;
@@ -720,7 +724,7 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
         }
         __syncwarp();
         mbar_arrive_if(lane == 0, &empty[slot]);  // the slot's data are no longer read
-        if (mt.kind == kUBlock && !publish(mt, kUBlock, true)) return;
+        if (kART && mt.kind == kUBlock && !publish(mt, kUBlock, true)) return;
         fold();
         if (mt.j == mt.nj - 1) write_partial(mt);
     }
@@ -1041,7 +1045,7 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
 // ---------------------------------------------------------------------------
 // the kernels
 // ---------------------------------------------------------------------------
-template <int D, int G>
+template <int D, int G, bool kART>
 __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     art_units_kernel(const Params p, const UParams up0, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv) {
@@ -1093,11 +1097,12 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     if (warp == 4) {
         producer_u<C>(p, up, ring, meta, full, empty, ctrl, &tk, &tv);
     } else if (warp == 5) {
-        stat_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
+        if (kART)
+            stat_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
                   reinterpret_cast<const float*>(smem + L.pmb), part_full, part_empty, rinfo,
                   reinterpret_cast<float*>(smem + L.ust), ctrl);
     } else {
-        consumer_u<C>(p, up, ring, meta, full, empty, part_full, part_empty, rinfo, L, smem, prank, ctrl);
+        consumer_u<C, kART>(p, up, ring, meta, full, empty, part_full, part_empty, rinfo, L, smem, prank, ctrl);
     }
 }
 
@@ -1128,10 +1133,10 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
     if (bad || n == 0 || t < 0 || t >= n) {
         if (!bad && n > 0 && lead) record_check(p.hdr, 261, item, t, n);
         if (w == 0) E::store(p.out, obase + d, 0.f);
-        if (lead) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
+        if (lead && p.blocks_used) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
         return;
     }
-    if (lead) p.blocks_used[item] = t + 1;
+    if (lead && p.blocks_used) p.blocks_used[item] = t + 1;
     const int kk = t / up.ck, sfirst = kk * up.ck;
     const bool use_fix = t != min(n, sfirst + up.ck) - 1;
     const int nunits = use_fix ? kk : kk + 1;        // whole units
@@ -1221,9 +1226,9 @@ inline int pick_ustages(int want, int smem_per_sm, int smem_per_block) {
     return 0;
 }
 
-template <int D, int G>
+template <int D, int G, bool kART>
 cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* li) {
-    auto kern = art_units_kernel<D, G>;
+    auto kern = art_units_kernel<D, G, kART>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1286,5 +1291,8 @@ cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* 
 
 }  // namespace art
 
-#define ART_UNITS_INSTANTIATE(D, G) \
-    template cudaError_t art::launch_units<D, G>(art::Params, art::UParams, cudaStream_t, art::LaunchInfo*);
+#define ART_UNITS_INSTANTIATE(D, G)                                                                      \
+    template cudaError_t art::launch_units<D, G, true>(art::Params, art::UParams, cudaStream_t,           \
+                                                       art::LaunchInfo*);                                 \
+    template cudaError_t art::launch_units<D, G, false>(art::Params, art::UParams, cudaStream_t,          \
+                                                        art::LaunchInfo*);
