@@ -39,6 +39,35 @@ struct PlanParams {
     int2* ulist;
 };
 
+// Exclusive prefix sum of one value per thread over the CTA's kPlanThreads
+// threads (warp shuffles, then the warp totals); `total` receives the sum.
+// `s_warp` holds kPlanThreads / 32 words of shared memory.
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* s_warp, long long& total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        long long t = lane < kPlanThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < kPlanThreads / 32) s_warp[lane] = t;  // inclusive warp totals
+    }
+    __syncthreads();
+    total = s_warp[kPlanThreads / 32 - 1];
+    const long long before = w > 0 ? s_warp[w - 1] : 0;
+    __syncthreads();  // s_warp may be reused by the caller right away
+    return before + x - v;
+}
+
 // One CTA per item: count the visit list (up to the first -1), check every
 // listed block and its pages, and record n and flags. The last CTA to finish
 // writes the claim order: items by visit-list length, longest first.
@@ -52,7 +81,7 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     __shared__ unsigned int bitmap[kBitmapWords];
     __shared__ int s_hist[kSortBuckets];
     __shared__ int s_part[kPlanThreads];
-    __shared__ int s_part2[kPlanThreads];
+    __shared__ long long s_warp[kPlanThreads / 32];
     __shared__ int s_n, s_flags, s_last, s_p0;
     const int item = blockIdx.x, tid = threadIdx.x;
     const int b = item / p.Hkv;
@@ -69,9 +98,14 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
         s_p0 = 0x7fffffff;
     }
     __syncthreads();
-    if (vrow)
+    if (vrow) {
+        // the first -1: a minimum per thread, per warp, then one shared atomic per warp
+        int first_end = 0x7fffffff;
         for (int pos = tid; pos < p.max_visit; pos += kPlanThreads)
-            if (vrow[pos] == -1) atomicMin(&s_n, pos);
+            if (vrow[pos] == -1) first_end = min(first_end, pos);
+        first_end = __reduce_min_sync(0xffffffffu, first_end);
+        if ((tid & 31) == 0 && first_end != 0x7fffffff) atomicMin(&s_n, first_end);
+    }
     __syncthreads();
     const int n = seq_ok ? s_n : 0;
     int err = seq_ok ? 0 : ART_STATUS_BAD_SEQLEN;
@@ -151,11 +185,9 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
             const int2 v = __ldcg(reinterpret_cast<const int2*>(&p.info[it]));
             part += (v.y & kItemBad) ? 0 : v.x;
         }
-        s_part2[tid] = part;
-        __syncthreads();
+        long long total = 0;
+        (void)block_exclusive_scan(part, s_warp, total);
         if (tid == 0) {
-            long long total = 0;
-            for (int i = 0; i < kPlanThreads; ++i) total += s_part2[i];
             const long long cap = (long long)kUnitBlocks * p.ctas;
             const long long waves = total > 0 ? (total + cap - 1) / cap : 1;
             long long ck = (total + waves * p.ctas - 1) / (waves * p.ctas);
@@ -180,18 +212,8 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
     constexpr int per = kSortBuckets / kPlanThreads;
     int sum = 0;
     for (int i = 0; i < per; ++i) sum += s_hist[tid * per + i];
-    s_part[tid] = sum;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int i = 0; i < kPlanThreads; ++i) {
-            const int t = s_part[i];
-            s_part[i] = run;
-            run += t;
-        }
-    }
-    __syncthreads();
-    int run = s_part[tid];
+    long long all_items = 0;
+    int run = (int)block_exclusive_scan(sum, s_warp, all_items);
     for (int i = 0; i < per; ++i) {
         const int t = s_hist[tid * per + i];
         s_hist[tid * per + i] = run;
@@ -230,20 +252,12 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
         chunk_sum += k < kmax ? s_hist[k] : 0;
     }
     __syncthreads();
-    s_part2[tid] = chunk_sum;
-    __syncthreads();
+    long long n_reg = 0;
+    int acc = (int)block_exclusive_scan(chunk_sum, s_warp, n_reg);
     if (tid == 0) {
-        int acc = 0;
-        for (int i = 0; i < kPlanThreads; ++i) {
-            const int t = s_part2[i];
-            s_part2[i] = acc;
-            acc += t;
-        }
-        p.hdr->n_regular = acc;
-        p.hdr->n_units = acc + (p.dense ? 0 : p.num_items * s_ck);  // then ck fix pieces per item
+        p.hdr->n_regular = (int)n_reg;
+        p.hdr->n_units = (int)n_reg + (p.dense ? 0 : p.num_items * s_ck);  // then ck fix pieces per item
     }
-    __syncthreads();
-    int acc = s_part2[tid];
     for (int i = 0; i < per; ++i) {
         const int k = tid * per + i;
         const int t = k < kmax ? s_hist[k] : 0;
