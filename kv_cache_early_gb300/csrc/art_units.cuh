@@ -140,13 +140,13 @@ struct URec {
 template <int D, int G>
 struct UCfg {
     using C = Cfg<true, D, G, 1>;
-    static constexpr int THREADS = 6 * 32;  // 4 consumer warps, producer, statistics
+    static constexpr int THREADS = 7 * 32;  // 4 consumer warps, producer, block summaries, tests
     static constexpr int W = C::SPL + 2;
     static_assert(W <= kUnitWords, "probe state fits the workspace words");
 };
 
 struct ULayout {
-    size_t meta, bars, part, plb, pmb, qt, ptab, rinfo, ust, ctrl, total;
+    size_t meta, bars, part, plb, pmb, qt, ptab, rinfo, ust, uhdr, uagg, ctrl, total;
 };
 
 template <int D, int G>
@@ -158,7 +158,7 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)stages * sizeof(UMeta);
     o = align_up(o, 16);
     L.bars = o;  // full[stages], empty[stages], part_full[NB], part_empty[NB]
-    o += (size_t)(2 * stages + 2 * kUnitRecs) * sizeof(uint64_t);
+    o += (size_t)(2 * stages + 2 * kUnitRecs + 2) * sizeof(uint64_t);  // ... then ufull, uempty
     o = align_up(o, 16);
     L.part = o;  // [NB][4 warps][PRW][PST] probe partial rows
     o += (size_t)kUnitRecs * C::GW * C::PRW * C::PST * sizeof(float);
@@ -177,9 +177,14 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o = align_up(o, 16);
     L.ust = o;  // [ck][W][32 lanes] block summaries of the unit being tested
     o += (size_t)kUnitBlocks * UCfg<D, G>::W * 32 * sizeof(float);
+    L.uhdr = o;  // the unit of the summaries
+    o += sizeof(URec);
     o = align_up(o, 16);
-    L.ctrl = o;
-    o += sizeof(Ctrl);
+    L.uagg = o;  // [W][32 lanes] its probe aggregate
+    o += (size_t)UCfg<D, G>::W * 32 * sizeof(float);
+    o = align_up(o, 16);
+    L.ctrl = o;  // only the abort and stop_item words of a Ctrl are used here
+    o += 128;
     L.total = align_up(o, 128) + 1024;  // room to align the ring to 1024 bytes
     return L;
 }
@@ -731,54 +736,169 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
 }
 
 // ---------------------------------------------------------------------------
-// statistics warp
+// helpers of the two statistics roles
+// ---------------------------------------------------------------------------
+// (M1, L1, O1) <- merge with (M2, L2, O2): the same softmax state over both sets of blocks
+template <int SPL>
+__device__ __forceinline__ void state_merge(float& M1, float& L1, float (&O1)[SPL], float M2, float L2,
+                                            const float (&O2)[SPL]) {
+    if (M2 == -INFINITY) return;
+    const float Mn = fmaxf(M1, M2);
+    const float a = exp2f(M1 - Mn), bw = exp2f(M2 - Mn);
+    L1 = fmaf(a, L1, bw * L2);
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) O1[j] = fmaf(a, O1[j], bw * O2[j]);
+    M1 = Mn;
+}
+
+// Probe slot s = lane + 32 j is word s of a partial row: head s % GP, rank s / GP; hs[j] is
+// its head, or -1 past the probe (heads from p.ph on are not part of it). All slots of a
+// lane belong to head hme.
+template <class C>
+__device__ __forceinline__ void probe_slots(const Params& p, int lane, int (&hs)[C::SPL], int& hme) {
+#pragma unroll
+    for (int j = 0; j < C::SPL; ++j) {
+        const int s = lane + 32 * j;
+        hs[j] = (s % C::GP < p.ph && s / C::GP < p.m) ? s % C::GP : -1;
+    }
+    hme = lane % C::GP < C::GQ ? lane % C::GP : 0;
+}
+
+// ---------------------------------------------------------------------------
+// summary warp: the consumers' block records become block summaries in the
+// unit store; at a unit's end it publishes the unit's probe aggregate and hands
+// the unit to the test warp
 // ---------------------------------------------------------------------------
 template <class C>
-__device__ void stat_u(const Params& p, const UParams& up, const float* part, const float* plb, const float* pmb,
-                       uint64_t* part_full, uint64_t* part_empty, const URec* rinfo, float* ust, Ctrl* ctrl) {
-    constexpr int G = C::GQ, SPL = C::SPL, NB = kUnitRecs, RGW = C::RGW;
+__device__ void summ_u(const Params& p, const UParams& up, const float* part, const float* plb, const float* pmb,
+                       uint64_t* part_full, uint64_t* part_empty, const URec* rinfo, float* ust, URec* uhdr,
+                       float* uagg, uint64_t* ufull, uint64_t* uempty, Ctrl* ctrl) {
+    constexpr int G = C::GQ, SPL = C::SPL, RGW = C::RGW, W = SPL + 2;
     constexpr int NPR = C::RGW * C::PRW;  // partial rows per record
-    constexpr int W = SPL + 2;
     constexpr int UW = 32 * kUnitWords;   // floats of one probe state in the workspace
     const int lane = threadIdx.x & 31;
-    const int m = p.m;
-    // probe slot s = lane + 32 j is word s of a partial row: head s % GP, rank s / GP;
-    // heads from p.ph on are not part of the probe
-    int hs[SPL];
-#pragma unroll
-    for (int j = 0; j < SPL; ++j) {
-        const int s = lane + 32 * j;
-        hs[j] = (s % C::GP < p.ph && s / C::GP < m) ? s % C::GP : -1;
-    }
-    const int hme = lane % C::GP < G ? lane % C::GP : 0;  // this lane's slots all belong to head hme
-
-    float Ma = -INFINITY, La = 0.f, Oa[SPL];  // aggregate of the unit's blocks so far
+    int hs[SPL], hme;
+    probe_slots<C>(p, lane, hs, hme);
+    float Ma = -INFINITY, La = 0.f, Oa[SPL];  // aggregate of the current unit's blocks
 #pragma unroll
     for (int j = 0; j < SPL; ++j) Oa[j] = 0.f;
-
-    // (M1, L1, O1) <- merge with (M2, L2, O2): the same softmax state over both sets of blocks
-    auto merge = [&](float& M1, float& L1, float (&O1)[SPL], float M2, float L2, const float (&O2)[SPL]) {
-        if (M2 == -INFINITY) return;
-        const float Mn = fmaxf(M1, M2);
-        const float a = exp2f(M1 - Mn), bw = exp2f(M2 - Mn);
-        L1 = fmaf(a, L1, bw * L2);
+    int urec = 0;  // units handed to the test warp
+    for (int rec = 0;; ++rec) {
+        const int rb = rec % kUnitRecs;
+        if (!wait_bounded(&part_full[rb], (uint32_t)(rec / kUnitRecs) & 1u, ctrl, p.hdr, 251)) return;
+        const URec ri = rinfo[rb];
+        const bool valid = ri.kind == kUBlock && ri.j >= 0 && ri.j < ri.nj && ri.nj <= up.ck && ri.item >= 0 &&
+                           ri.item < p.num_items && ri.k >= 0 && ri.k < up.maxk;
+        // a new unit (or the end) needs the summary buffer back from the test warp
+        if ((!valid || ri.j == 0) && urec >= 1 &&
+            !wait_bounded(uempty, (uint32_t)(urec - 1) & 1u, ctrl, p.hdr, 255))
+            return;
+        if (!valid) {
+            if (ri.kind == kUBlock && lane == 0) record_check(p.hdr, 254, ri.item, ri.k, ri.j);
+            URec e = ri;
+            e.kind = kUEnd;
+            if (lane == 0) *uhdr = e;
+            __syncwarp();
+            mbar_arrive_if(lane == 0, ufull);
+            return;
+        }
+        // block max and weight sum of this lane's head over the 4 warps (each used its own
+        // max), and the block's probe sums at that max
+        float sw[RGW];
+        float mbk = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < SPL; ++j) O1[j] = fmaf(a, O1[j], bw * O2[j]);
-        M1 = Mn;
-    };
-
-    auto finish_unit = [&](int item, int k, int nj) -> bool {
-        const size_t iu = (size_t)item * up.maxk + k;
-        {
+        for (int w = 0; w < RGW; ++w) {
+            sw[w] = pmb[(rb * RGW + w) * G + hme];
+            mbk = fmaxf(mbk, sw[w]);
+        }
+        float lb = 0.f;
+#pragma unroll
+        for (int w = 0; w < RGW; ++w) {
+            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a warp without valid keys adds nothing
+            lb = fmaf(sw[w], plb[(rb * RGW + w) * G + hme], lb);
+        }
+        const float* pp = part + (size_t)rb * NPR * C::PST;
+        float pb[SPL];
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < RGW; ++w) {
+                float pw = 0.f;
+#pragma unroll
+                for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
+                v = fmaf(sw[w], pw, v);
+            }
+            pb[j] = hs[j] >= 0 ? v : 0.f;  // slots past the probe hold no data
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, &part_empty[rb]);
+        float* sm = ust + (size_t)ri.j * W * 32;
+        sm[lane] = mbk;
+        sm[32 + lane] = lb;
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) sm[(2 + j) * 32 + lane] = pb[j];
+        if (ri.j == 0) {
+            Ma = mbk;
+            La = lb;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) Oa[j] = pb[j];
+        } else {
+            state_merge<SPL>(Ma, La, Oa, mbk, lb, pb);
+        }
+        if (ri.j == ri.nj - 1) {
+            // the unit's aggregate for the look-backs of later units, and for the test warp
+            const size_t iu = (size_t)ri.item * up.maxk + ri.k;
             float* ga = up.agg + iu * UW;
             ga[lane] = Ma;
             ga[32 + lane] = La;
 #pragma unroll
             for (int j = 0; j < SPL; ++j) ga[(2 + j) * 32 + lane] = Oa[j];
+            uagg[lane] = Ma;
+            uagg[32 + lane] = La;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) uagg[(2 + j) * 32 + lane] = Oa[j];
+            if (lane == 0) *uhdr = ri;
+            __syncwarp();
+            mbar_arrive_if(lane == 0, ufull);
+            ++urec;
             fence_acq_rel_gpu();
             __syncwarp();
             if (lane == 0) st_release_gpu(&up.tflag[iu], 1);
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// test warp: per unit handed over by the summary warp, the look-back for the
+// probe state before the unit, the stability tests of its blocks, and its stop
+// ---------------------------------------------------------------------------
+template <class C>
+__device__ void stat_u(const Params& p, const UParams& up, const float* ust, const URec* uhdr, const float* uagg,
+                       uint64_t* ufull, uint64_t* uempty, Ctrl* ctrl) {
+    bool released = false;  // the summary buffer has been handed back for the next unit
+    auto release_buffer = [&]() {
+        if (released) return;
+        __syncwarp();
+        mbar_arrive_if((threadIdx.x & 31) == 0, uempty);
+        released = true;
+    };
+    constexpr int SPL = C::SPL;
+    constexpr int W = SPL + 2;
+    constexpr int UW = 32 * kUnitWords;  // floats of one probe state in the workspace
+    const int lane = threadIdx.x & 31;
+    int hs[SPL], hme;
+    probe_slots<C>(p, lane, hs, hme);
+    (void)hme;
+
+    auto finish_unit = [&](int item, int k, int nj, const float* us) -> bool {
+        const size_t iu = (size_t)item * up.maxk + k;
+        // the unit's own aggregate, handed over by the summary warp with the summaries
+        float Ma, La, Oa[SPL];
+        Ma = uagg[lane];
+        La = uagg[32 + lane];
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) Oa[j] = uagg[(2 + j) * 32 + lane];
         // the probe state before this unit: aggregates of the earlier units, back to the
         // nearest one with an inclusive state
         float cM = -INFINITY, cL = 0.f, cO[SPL];
@@ -841,7 +961,7 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
                         for (int j = 0; j < SPL; ++j) O2[q][j] = ft[q] ? __ldcg(src + (2 + j) * 32 + lane) : 0.f;
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) merge(cM, cL, cO, M2[q], L2[q], O2[q]);
+                    for (int q = 0; q < 4; ++q) state_merge<SPL>(cM, cL, cO, M2[q], L2[q], O2[q]);
                 }
                 if (e < take) break;  // reached an inclusive state or the list's start
                 kk -= take;
@@ -858,7 +978,7 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
                 float iM = cM, iL = cL, iO[SPL];
 #pragma unroll
                 for (int j = 0; j < SPL; ++j) iO[j] = cO[j];
-                merge(iM, iL, iO, Ma, La, Oa);
+                state_merge<SPL>(iM, iL, iO, Ma, La, Oa);
                 // its flag follows after the tests' first pass, when these stores are done
                 float* gi = up.incl + iu * UW;
                 gi[lane] = iM;
@@ -879,12 +999,16 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
             const float n0 = sqrtf(q);  // |x| before the unit's first block
             // pass 1, lane-local: the probe's change over each block (the update of x is
             // per slot), and this lane's terms of sum delta^2, sum delta . x_{i-1}, |x_i|^2
-            float v[4 * kUnitBlocks];
+            constexpr int VS = 16;  // entries per statistic (>= kUnitBlocks; 4 VS a power of two)
+            static_assert(VS >= kUnitBlocks, "one entry per block");
+            float v[4 * VS];
+#pragma unroll
+            for (int j = 0; j < 4 * VS; ++j) v[j] = 0.f;
 #pragma unroll
             for (int j = 0; j < kUnitBlocks; ++j) {
                 float s1 = 0.f, s2 = 0.f, s3 = 0.f;
                 if (j < nj) {
-                    const float* s = ust + (size_t)j * W * 32;
+                    const float* s = us + (size_t)j * W * 32;
                     const float mbk = s[lane], lb = s[32 + lane];
                     const float Mn = fmaxf(M, mbk);
                     const float a = exp2f(M - Mn);
@@ -904,16 +1028,16 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
                     }
                 }
                 v[j] = s1;
-                v[kUnitBlocks + j] = s2;
-                v[2 * kUnitBlocks + j] = s3;
-                v[3 * kUnitBlocks + j] = 0.f;
+                v[VS + j] = s2;
+                v[2 * VS + j] = s3;
             }
+            release_buffer();  // the summaries are read: the summary warp may fill in the next unit's
             fence_acq_rel_gpu();
             __syncwarp();
             if (lane == 0) st_release_gpu(&up.tflag[iu], 2);  // the inclusive state
             // pass 2: the warp sums of all of them at once; lane l then holds the sums of
             // entries 2 l and 2 l + 1
-            transpose_reduce<4 * kUnitBlocks, 32>(v, lane);
+            transpose_reduce<4 * VS, 32>(v, lane);
             auto sum_at = [&](int entry) -> float {  // warp sum of entry `entry`, in every lane
                 const float a0 = __shfl_sync(0xffffffffu, v[0], (entry >> 1) & 31);
                 const float a1 = __shfl_sync(0xffffffffu, v[1], (entry >> 1) & 31);
@@ -922,8 +1046,8 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
             // pass 3: lane b takes the test of block b, the same tests as the one-CTA
             // statistics warp, multiplied through by their positive denominators
             const int bj = lane < kUnitBlocks ? lane : 0;
-            const float s1 = sum_at(bj), s2 = sum_at(kUnitBlocks + bj), s3 = sum_at(2 * kUnitBlocks + bj);
-            const float s3p = sum_at(2 * kUnitBlocks + (bj > 0 ? bj - 1 : 0));
+            const float s1 = sum_at(bj), s2 = sum_at(VS + bj), s3 = sum_at(2 * VS + bj);
+            const float s3p = sum_at(2 * VS + (bj > 0 ? bj - 1 : 0));
             const float nprev = bj == 0 ? n0 : sqrtf(s3p);
             const float rprev = bj == 0 ? (n0 > 0.f ? 1.f / n0 : 0.f) : __fdividef(1.f, nprev);
             const float ni = sqrtf(s3);
@@ -981,64 +1105,14 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* part, co
         return true;
     };
 
-    for (int rec = 0;; ++rec) {
-        const int rb = rec % NB;
-        if (!wait_bounded(&part_full[rb], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 251)) return;
-        const URec ri = rinfo[rb];
+    for (int uu = 0;; ++uu) {
+        if (!wait_bounded(ufull, (uint32_t)uu & 1u, ctrl, p.hdr, 251)) return;
+        const URec ri = *uhdr;
         if (ri.kind != kUBlock) return;
-        if (ri.j < 0 || ri.j >= ri.nj || ri.nj > up.ck || ri.item < 0 || ri.item >= p.num_items || ri.k < 0 ||
-            ri.k >= up.maxk) {
-            if (lane == 0) record_check(p.hdr, 254, ri.item, ri.k, ri.j);
-            return;
-        }
-        // block max and weight sum of this lane's head over the 4 warps (each used its own max),
-        // and the block's probe sums at that max
-        float sw[RGW];
-        float mbk = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < RGW; ++w) {
-            sw[w] = pmb[(rb * RGW + w) * G + hme];
-            mbk = fmaxf(mbk, sw[w]);
-        }
-        float lb = 0.f;
-#pragma unroll
-        for (int w = 0; w < RGW; ++w) {
-            sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a warp without valid keys adds nothing
-            lb = fmaf(sw[w], plb[(rb * RGW + w) * G + hme], lb);
-        }
-        const float* pp = part + (size_t)rb * NPR * C::PST;
-        float pb[SPL];
-#pragma unroll
-        for (int j = 0; j < SPL; ++j) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < RGW; ++w) {
-                float pw = 0.f;
-#pragma unroll
-                for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
-                v = fmaf(sw[w], pw, v);
-            }
-            pb[j] = hs[j] >= 0 ? v : 0.f;  // slots past the probe hold no data
-        }
-        __syncwarp();
-        mbar_arrive_if(lane == 0, &part_empty[rb]);
-        float* s = ust + (size_t)ri.j * W * 32;
-        s[lane] = mbk;
-        s[32 + lane] = lb;
-#pragma unroll
-        for (int j = 0; j < SPL; ++j) s[(2 + j) * 32 + lane] = pb[j];
-        if (ri.j == 0) {
-            Ma = mbk;
-            La = lb;
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) Oa[j] = pb[j];
-        } else {
-            merge(Ma, La, Oa, mbk, lb, pb);
-        }
-        if (ri.j == ri.nj - 1) {
-            __syncwarp();
-            if (!finish_unit(ri.item, ri.k, ri.nj)) return;
-        }
+        released = false;
+        const bool done = finish_unit(ri.item, ri.k, ri.nj, ust);
+        release_buffer();  // a unit whose item had stopped before it has not read its summaries
+        if (!done) return;
     }
 }
 
@@ -1061,6 +1135,8 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     uint64_t* empty = full + p.stages;
     uint64_t* part_full = empty + p.stages;
     uint64_t* part_empty = part_full + kUnitRecs;
+    uint64_t* ufull = part_empty + kUnitRecs;
+    uint64_t* uempty = ufull + 1;
     int* prank = reinterpret_cast<int*>(smem + L.ptab);
     URec* rinfo = reinterpret_cast<URec*>(smem + L.rinfo);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
@@ -1074,6 +1150,8 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
             mbar_init(&part_full[b], C::GW);
             mbar_init(&part_empty[b], 1);
         }
+        mbar_init(ufull, 1);
+        mbar_init(uempty, 1);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
         fence_mbar_init();
@@ -1098,9 +1176,14 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
         producer_u<C>(p, up, ring, meta, full, empty, ctrl, &tk, &tv);
     } else if (warp == 5) {
         if (kART)
-            stat_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
-                  reinterpret_cast<const float*>(smem + L.pmb), part_full, part_empty, rinfo,
-                  reinterpret_cast<float*>(smem + L.ust), ctrl);
+            summ_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
+                      reinterpret_cast<const float*>(smem + L.pmb), part_full, part_empty, rinfo,
+                      reinterpret_cast<float*>(smem + L.ust), reinterpret_cast<URec*>(smem + L.uhdr),
+                      reinterpret_cast<float*>(smem + L.uagg), ufull, uempty, ctrl);
+    } else if (warp == 6) {
+        if (kART)
+            stat_u<C>(p, up, reinterpret_cast<const float*>(smem + L.ust), reinterpret_cast<const URec*>(smem + L.uhdr),
+                      reinterpret_cast<const float*>(smem + L.uagg), ufull, uempty, ctrl);
     } else {
         consumer_u<C, kART>(p, up, ring, meta, full, empty, part_full, part_empty, rinfo, L, smem, prank, ctrl);
     }
