@@ -118,3 +118,22 @@ def test_workspace_size(lib):
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, 7):
         assert lib.art_status_string(code)
+
+
+def test_decode_path_choice(lib, monkeypatch):
+    """Which kernel path a call takes (host logic only: with ART_UNITS set the
+    choice needs no device). The unit path is offered for bf16 with at most 256
+    items, patience at most 16 and a workspace that holds its area."""
+    monkeypatch.setenv("ART_UNITS", "1")
+    small = good_shape(batch=3, num_kv_heads=4, num_q_heads=16)  # bf16, 12 items
+    ws = K.art_workspace_bytes(small)
+    assert K.art_decode_path(small, 2, ws) == 1
+    assert K.art_decode_path(small, 16, ws) == 1
+    assert K.art_decode_path(small, 17, ws) == 0  # patience beyond the longest unit
+    assert K.art_decode_path(small, 2, 64 + 12 * 12) == 0  # the one-CTA path's workspace only
+    assert K.art_decode_path(good_shape(batch=3, num_kv_heads=4, num_q_heads=16, dtype=1), 2, 1 << 30) == 0
+    big = good_shape(batch=300, num_kv_heads=1, num_q_heads=1)  # 300 items
+    assert K.art_decode_path(big, 2, 1 << 30) == 0
+    assert K.art_decode_path(good_shape(head_dim=96), 2, 1 << 30) == 0  # fails the shape checks
+    monkeypatch.setenv("ART_UNITS", "0")
+    assert K.art_decode_path(small, 2, ws) == 0
