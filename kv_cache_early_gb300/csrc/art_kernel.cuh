@@ -115,6 +115,7 @@ struct Cfg {
     static_assert(!TC || NG < 3 || XGB >= (G * D + 2 * G) * 4, "merge area fits the exchange area");
     static constexpr int KS = D / 16;            // tensor-core k-steps (QK) and m-tiles (PV)
     static constexpr bool LAG = G <= 4;          // decision one block behind (register budget)
+    static constexpr bool HINT = TC && NG >= 3;  // bounded waits with a long suspend-time hint
     static_assert(LPR >= 8 && LPR <= 32 && EPC >= 2 && EPC <= 8, "row must be 128..512 bytes");
     static_assert(RW % RPW == 0 && NI >= 1, "rows per warp");
     static_assert(TC || 32 % RW == 0, "softmax lane groups");
@@ -213,21 +214,29 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Waits for the phase with `parity` of `bar` to complete, warp-uniformly. The
-// threads sleep in mbarrier.try_wait (woken by the phase completing) rather
-// than spin. Returns false (and sets ART_STATUS_TIMEOUT) when the wait exceeds
-// kWaitLimitNs. Only a warp's own wait ends it: the warps of a consumer group
-// always wait on the same barrier phases, so they give up together and none is
-// left behind in a named barrier.
+// Waits for the phase with `parity` of `bar` to complete, warp-uniformly.
+// kHint: the threads sleep in mbarrier.try_wait with a long suspend-time hint
+// (woken by the phase completing); otherwise they wait in plain try_wait (a
+// potentially blocking test that returns at the phase's completion or after the
+// hardware's own short time limit). Measured: the hint is 0.5 % faster with one
+// CTA per SM running three or four consumer groups, plain try_wait 2-3 % faster
+// with two CTAs per SM. Returns false (and sets ART_STATUS_TIMEOUT) when the wait
+// exceeds kWaitLimitNs. Only a warp's own wait ends it: the warps of a consumer
+// group always wait on the same barrier phases, so they give up together and
+// none is left behind in a named barrier.
+template <bool kHint = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctrl* ctrl, WsHeader* hdr,
                                              int where = 0) {
     constexpr uint32_t kSleepNs = 200000;  // upper bound of one sleep; the limit is checked between sleeps
-    // a phase that has completed already costs one test, not a (slower) suspending wait
+    auto try_once = [&]() -> bool {
+        return kHint ? mbar_try_wait_sleep(bar, parity, kSleepNs) : mbar_try_wait(bar, parity);
+    };
+    // a phase that has completed already costs one test
     if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
-    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
+    if (__all_sync(0xffffffffu, try_once())) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepNs))) return true;
+        if (__all_sync(0xffffffffu, try_once())) return true;
         int late = (threadIdx.x & 31) == 0 && global_ns() - t0 > kWaitLimitNs;
         if (__any_sync(0xffffffffu, late)) {
             if ((threadIdx.x & 31) == 0) {
@@ -256,7 +265,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
 
     auto acquire = [&]() -> bool {
         if (have_slot) return true;
-        if (!wait_bounded(&empty[slot], (round & 1u) ^ 1u, ctrl, p.hdr, 131)) return false;
+        if (!wait_bounded<C::HINT>(&empty[slot], (round & 1u) ^ 1u, ctrl, p.hdr, 131)) return false;
         have_slot = true;
         return true;
     };
@@ -503,7 +512,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
     reset();
     for (int v = 0;; ++v) {
         const int vb = v % NB;
-        if (!wait_bounded(&part_full[vb], (uint32_t)(v / NB) & 1u, ctrl, p.hdr, 141)) return;
+        if (!wait_bounded<C::HINT>(&part_full[vb], (uint32_t)(v / NB) & 1u, ctrl, p.hdr, 141)) return;
         const SlotMeta* info = &ctrl->info[vb];
         const int kind = info->kind, item = info->item;
         if (kind == kSlotEnd) return;
@@ -679,7 +688,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     auto cbar_sync = [&]() -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(cbar);
-        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr);
+        const bool r = wait_bounded<C::HINT>(cbar, cbph, ctrl, p.hdr);
         cbph ^= 1u;
         return r;
     };
@@ -701,7 +710,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
         return v++;
     };
     auto wait_dec = [&](int rec) -> int {
-        if (!wait_bounded(&dec_bar[rec & 1], (uint32_t)(rec >> 1) & 1u, ctrl, p.hdr)) return -1;
+        if (!wait_bounded<C::HINT>(&dec_bar[rec & 1], (uint32_t)(rec >> 1) & 1u, ctrl, p.hdr)) return -1;
         return ctrl->dec[rec & 1];
     };
     auto fold = [&](const uint64_t (&t)[G][E2], const float* mb, const float* lb) {
@@ -777,7 +786,7 @@ __device__ void consumer_warps(const Params& p, unsigned char* ring, const SlotM
     };
 
     for (;;) {
-        if (!wait_bounded(&full[slot], round & 1u, ctrl, p.hdr)) return;
+        if (!wait_bounded<C::HINT>(&full[slot], round & 1u, ctrl, p.hdr)) return;
         const SlotMeta mt = meta[slot];
         if (mt.kind == kSlotEnd) {
             if (LAG && pending && !resolve_pending()) return;
@@ -1104,7 +1113,7 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
     auto cbar_sync = [&]() -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(cbar);
-        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr, 111 + gi);
+        const bool r = wait_bounded<C::HINT>(cbar, cbph, ctrl, p.hdr, 111 + gi);
         cbph ^= 1u;
         return r;
     };
@@ -1112,7 +1121,7 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
         return ((size_t)b * p.Hq + (size_t)g * G + h) * D + col;
     };
     auto wait_dec = [&](int rec) -> int {
-        if (!wait_bounded(&dec_bar[rec % NB], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 121 + gi)) return -1;
+        if (!wait_bounded<C::HINT>(&dec_bar[rec % NB], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 121 + gi)) return -1;
         return ctrl->dec[rec % NB];
     };
     auto fold = [&](const float (&t)[KS][4], const float* mb, const float* lb) {
@@ -1221,9 +1230,9 @@ __device__ void consumer_tc(const Params& p, unsigned char* ring, const SlotMeta
             // the slot's previous entry belongs to another group and its copies may land
             // after this group's own earlier entries: wait until it has been consumed, so
             // that the parity test below cannot match that older fill
-            if (!wait_bounded(&empty[slot], (uint32_t)(u / p.stages - 1) & 1u, ctrl, p.hdr, 151 + gi)) return;
+            if (!wait_bounded<C::HINT>(&empty[slot], (uint32_t)(u / p.stages - 1) & 1u, ctrl, p.hdr, 151 + gi)) return;
         }
-        if (!wait_bounded(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
+        if (!wait_bounded<C::HINT>(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
         SlotMeta mt = meta[slot];
         if (mt.kind < 0 || mt.kind > kSlotPad ||
             (mt.kind == kSlotBlock && (mt.item < 0 || mt.item >= p.num_items || mt.nvalid < 1 || mt.nvalid > kBK ||
@@ -1522,7 +1531,7 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
     auto cbar_sync = [&]() -> bool {
         __syncwarp();
         mbar_arrive_if(lane == 0, cbar);
-        const bool r = wait_bounded(cbar, cbph, ctrl, p.hdr, 111 + gi);
+        const bool r = wait_bounded<C::HINT>(cbar, cbph, ctrl, p.hdr, 111 + gi);
         cbph ^= 1u;
         return r;
     };
@@ -1530,7 +1539,7 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
         return ((size_t)b * p.Hq + (size_t)g * G + h) * D + col;
     };
     auto wait_dec = [&](int rec) -> int {
-        if (!wait_bounded(&dec_bar[rec % NB], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 121 + gi)) return -1;
+        if (!wait_bounded<C::HINT>(&dec_bar[rec % NB], (uint32_t)(rec / NB) & 1u, ctrl, p.hdr, 121 + gi)) return -1;
         return ctrl->dec[rec % NB];
     };
     auto fold = [&](const float (&t)[MT][4], const float* mb, const float* lb) {
@@ -1662,9 +1671,9 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
             // the slot's previous entry belongs to another group and its copies may land
             // after this group's own earlier entries: wait until it has been consumed, so
             // that the parity test below cannot match that older fill
-            if (!wait_bounded(&empty[slot], (uint32_t)(u / p.stages - 1) & 1u, ctrl, p.hdr, 151 + gi)) return;
+            if (!wait_bounded<C::HINT>(&empty[slot], (uint32_t)(u / p.stages - 1) & 1u, ctrl, p.hdr, 151 + gi)) return;
         }
-        if (!wait_bounded(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
+        if (!wait_bounded<C::HINT>(&full[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 101 + gi)) return;
         SlotMeta mt = meta[slot];
         if (mt.kind < 0 || mt.kind > kSlotPad ||
             (mt.kind == kSlotBlock && (mt.item < 0 || mt.item >= p.num_items || mt.nvalid < 1 || mt.nvalid > kBK ||
