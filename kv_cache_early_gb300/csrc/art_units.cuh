@@ -51,6 +51,8 @@
 // waits on another unit, so the waits end. They are bounded all the same.
 #pragma once
 
+#include <cstddef>
+
 #include "art_kernel.cuh"
 
 namespace art {
@@ -184,6 +186,8 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)UCfg<D, G>::W * 32 * sizeof(float);
     o = align_up(o, 16);
     L.ctrl = o;  // only the abort and stop_item words of a Ctrl are used here
+    static_assert(offsetof(Ctrl, abort) + sizeof(int) <= 128 && offsetof(Ctrl, stop_item) + sizeof(int) <= 128,
+                  "the words of Ctrl used by the unit kernel fit its 128 bytes");
     o += 128;
     L.total = align_up(o, 128) + 1024;  // room to align the ring to 1024 bytes
     return L;
