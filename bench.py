@@ -7,15 +7,22 @@ in HBM. Prints one JSON line (rank 0) with queries/s, the HBM roofline of the
 decode kernel, the dense twin, the CPU oracle baseline, clocks and an
 end-to-end figure through the public API with host buffers.
 
-Default workload: the Llama-3-8B-shaped decode layer (batch 16, 32 query /
-8 KV heads, d=128, 32768-token context, bf16, KV block 64, planted keys,
-sink-first most-recent-first order, eps 1e-3, patience 2).
+Default workload: the ragged batch (64 sequences of 1k-64k tokens, 32 query /
+8 KV heads, d=128, bf16, 16-token pages placed by a seeded permutation, 5 % of
+the blocks with values x8, sink-first most-recent-first order, eps 1e-3,
+patience 2), the largest of the five decode workloads (about 8.7 GB of listed
+K and V).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config 1..5] [--eps E] [--patience P] [--no-cpu-baseline]
-Under torchrun (N > 1) every rank runs its own independently seeded copy of
-the workload (weak scaling, no collective on the data path); the timing is
-the max over ranks.
+                  [--shard sequences|replicas] [--diag]
+Under torchrun (N > 1) the default (--shard sequences) partitions the one
+seeded workload by sequence: rank r owns a contiguous slice of the sequences
+with their block-table rows and the pages they name (strong scaling, no
+collective on the data path; the step time is the max over ranks).
+--shard replicas runs a full copy of the workload on every rank instead (weak
+scaling). --diag prints the convergence and score-versus-contribution
+diagnostics instead of the benchmark line.
 """
 from __future__ import annotations
 
@@ -42,7 +49,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--shard", default="sequences", choices=["sequences", "replicas"],
+                    help="N > 1: partition the workload's sequences over the ranks, or run a replica per rank")
+    ap.add_argument("--diag", action="store_true",
+                    help="print the convergence (O^(t) vs O^(T)) and score-vs-contribution diagnostics")
     ap.add_argument("--eps", type=float, default=None)
     ap.add_argument("--patience", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
@@ -225,11 +236,13 @@ def cpu_baseline(w, eps, p, budget_s=12.0):
             "seconds_per_run": t}
 
 
-def config_dict(w, eps, p, ws):
+def config_dict(w, eps, p, ws, shard="sequences"):
+    par = "single GPU" if ws == 1 else (f"partition by sequence over {ws} GPUs" if shard == "sequences"
+                                        else f"{ws} independent replicas")
     return {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "page_size": w.page_size, "block_size": w.block_size, "eps": eps,
             "patience": p, "l2": "flushed (256 MB write) before every timed call; inputs also exceed L2",
-            "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"}
+            "parallelism": par}
 
 
 # ---------------------------------------------------------------------------
@@ -286,10 +299,14 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     B.build()
-    w = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)  # one replica per rank
+    w_all = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)
+    sharded = ws > 1 and args.shard == "sequences"
+    # partition by sequence: this rank's slice of the one seeded workload; else a replica
+    w = W.shard_sequences(w_all, rank, ws) if sharded else w_all
     eps, p = w.eps_mag, w.patience
     dev = K.DeviceInputs(w)
-    queries = w.batch * w.num_q_heads
+    queries = w.batch * w.num_q_heads  # this rank's
+    queries_job = w_all.batch * w.num_q_heads if sharded else ws * queries
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > L2 (126 MB)
 
@@ -343,7 +360,7 @@ def run_ours(args):
     clocks = clk.stop()
     ms = max_over_ranks(float(t_art.mean()), device="cuda")
     ms_kernel = max_over_ranks(float(t_kern.mean()), device="cuda")
-    value = ws * queries / (ms * 1e-3)
+    value = queries_job / (ms * 1e-3)
 
     # dense twin on the same buffers
     dense = None
@@ -373,6 +390,7 @@ def run_ours(args):
     achieved = alg / (ms_kernel * 1e-3) / 1e9
     traffic, traffic_src = load_traffic(w.name, alg, "units" if path == 1 else "one CTA per item")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "frac_of_8tbs": achieved / 8000.0,
                 "traffic": traffic, "traffic_source": traffic_src, "peak_kind": peak_kind,
                 "kernel": kernels, "path": "units" if path == 1 else "one CTA per item",
                 "algorithmic_bytes_per_launch": alg,
@@ -409,7 +427,8 @@ def run_ours(args):
             e2e_step()
         t_e = time_calls(e2e_step, args.steps)
         ms_e = float(t_e.mean())
-        e2e = {"value": ws * queries / (ms_e * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
+        ms_e = max_over_ranks(ms_e, device="cuda")
+        e2e = {"value": queries_job / (ms_e * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e,
                "note": "KV cache resident on the device; per-step inputs and outputs copied"}
 
@@ -456,9 +475,9 @@ def run_ours(args):
         n = w.visit_lengths()
         line = {"metric": "decode-attention queries/s (ART)", "value": value, "unit": "queries/s",
                 "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "higher_is_better": True, "scaling": "strong" if sharded else "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-                "config": config_dict(w, eps, p, ws),
+                "config": config_dict(w_all, eps, p, ws, args.shard),
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": (3 if path == 1 else 2) * args.steps,
                 "dense_twin": dense,
@@ -472,8 +491,118 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# diagnostics: convergence of O^(t) and attention score vs value contribution
+# ---------------------------------------------------------------------------
+def _ranks(x):
+    r = np.empty(x.size, dtype=np.float64)
+    r[np.argsort(x, kind="stable")] = np.arange(x.size)
+    return r
+
+
+def score_vs_contribution(w, items, top=0.01):
+    """Per sampled item, over its tokens t: the attention score a_t = max over the
+    group's query heads of the softmax weight alpha_{h,t}, and the contribution
+    c_t = max over those heads of |alpha_{h,t} v_t|_2 (the norm of token t's term in
+    the head's output) -- the two rankings the ART paper compares (sec. 1, Fig. 1).
+    Returns the Spearman rank correlation of a and c, the share of the top `top`
+    tokens by contribution that are also in the top `top` by score, and the same
+    share restricted to tokens of the value-boosted blocks."""
+    G, d = w.group, w.head_dim
+    rho, overlap, boosted_hit = [], [], []
+    for it in items:
+        b, g = divmod(int(it), w.num_kv_heads)
+        N = int(w.seq_lens[b])
+        toks = np.arange(N)
+        pg, row = w.block_table[b, toks // w.page_size], toks % w.page_size
+        kk = W.as_f32(w.k_cache[pg, g, row, :], w.dtype).astype(np.float64)
+        vv = W.as_f32(w.v_cache[pg, g, row, :], w.dtype).astype(np.float64)
+        qq = W.as_f32(w.q[b, g * G:(g + 1) * G], w.dtype).astype(np.float64)
+        s = qq @ kk.T / np.sqrt(d)
+        a = np.exp(s - s.max(axis=1, keepdims=True))
+        a /= a.sum(axis=1, keepdims=True)
+        vn = np.linalg.norm(vv, axis=1)
+        score = a.max(axis=0)
+        contrib = (a * vn[None, :]).max(axis=0)
+        rs, rc = _ranks(score), _ranks(contrib)
+        rho.append(float(np.corrcoef(rs, rc)[0, 1]))
+        k = max(1, int(round(top * N)))
+        ts, tc = set(np.argsort(-score)[:k].tolist()), np.argsort(-contrib)[:k]
+        overlap.append(len(ts.intersection(tc.tolist())) / k)
+        big = vn > 2.0 * np.median(vn)  # the x8 blocks
+        tcb = [t for t in tc.tolist() if big[t]]
+        if tcb:
+            boosted_hit.append(sum(t in ts for t in tcb) / len(tcb))
+    return {"items": [int(i) for i in items], "spearman_score_vs_contribution": float(np.mean(rho)),
+            "top_frac": top, "top_overlap": float(np.mean(overlap)),
+            "boosted_top_contrib_share_in_top_score": float(np.mean(boosted_hit)) if boosted_hit else None}
+
+
+def run_diag(args):
+    """The convergence curve: rel-L2(O^(t), O^(T)) against the loaded fraction t / n
+    of the visit list (sink first, then most recent first), per item, binned; O^(t)
+    from libart forced to stop after t blocks (eps = +inf, patience t - 1), O^(T)
+    from the dense twin. Then the ART stop at eps 1e-3, patience 2, and the score
+    versus contribution ranks on the ragged workload."""
+    import torch
+
+    import kv_cache_early_gb300 as K
+    from kv_cache_early_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(0)
+    res = {"diag": "convergence of O^(t) and score vs contribution", "configs": {}}
+    for cfg in (2, 4):
+        w = W.config(cfg)
+        dev = K.DeviceInputs(w)
+        n = w.visit_lengths()
+        shp = (w.num_items, w.group * w.head_dim)
+        dev.dense()
+        torch.cuda.synchronize()
+        OT = dev.out.float().cpu().numpy().reshape(shp).astype(np.float64)
+        nT = np.linalg.norm(OT, axis=1)
+        fr, rel = [], []
+        t = 2
+        while t <= int(n.max()):
+            dev.art(float("inf"), float("inf"), t - 1)
+            torch.cuda.synchronize()
+            bu = dev.blocks_used.cpu().numpy().reshape(-1)
+            assert (bu == np.minimum(n, t)).all(), "forced stop"
+            Ot = dev.out.float().cpu().numpy().reshape(shp).astype(np.float64)
+            live = n >= t  # items whose list is not yet exhausted
+            fr.append((t / n)[live])
+            rel.append((np.linalg.norm(Ot - OT, axis=1) / nT)[live])
+            t *= 2
+        fr, rel = np.concatenate(fr), np.concatenate(rel)
+        edges = [0.0, 1 / 64, 1 / 32, 1 / 16, 1 / 8, 1 / 4, 1 / 2, 1.0001]
+        curve = []
+        for lo, hi in zip(edges, edges[1:]):
+            m = (fr > lo) & (fr <= hi)
+            if m.any():
+                curve.append({"loaded_frac": [lo, min(hi, 1.0)], "points": int(m.sum()),
+                              "rel_l2_median": float(np.median(rel[m])), "rel_l2_p90": float(np.percentile(rel[m], 90))})
+        dev.art(1e-3, 1e-3, 2)
+        torch.cuda.synchronize()
+        bu = dev.blocks_used.cpu().numpy().reshape(-1)
+        Oa = dev.out.float().cpu().numpy().reshape(shp).astype(np.float64)
+        ra = np.linalg.norm(Oa - OT, axis=1) / nT
+        entry = {"workload": w.name, "curve": curve,
+                 "art_eps1e-3_p2": {"loaded_frac_mean": float((bu / n).mean()),
+                                    "rel_l2_median": float(np.median(ra)), "rel_l2_max": float(ra.max())}}
+        if cfg == 4:
+            rng = np.random.default_rng(0)
+            entry["score_vs_contribution"] = score_vs_contribution(
+                w, np.sort(rng.choice(w.num_items, size=8, replace=False)))
+        res["configs"][str(cfg)] = entry
+        del dev
+        torch.cuda.empty_cache()
+    print(json.dumps(res))
+
+
 def main():
     args = parse()
+    if args.diag:
+        run_diag(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -199,19 +199,28 @@ int dense_decode(const void* q, const void* k_cache, const void* v_cache,
  * device allocator.
  *   Limit: batch * num_kv_heads <= 16384; larger calls return
  *          ART_ERR_UNSUPPORTED without touching the device.
- *   Set-up: a device's first call looks up the array's device address
- *          (cudaGetSymbolAddress) with that device current; make that first
- *          call before any stream capture.
+ *   Set-up: every call looks up the array's device address on the current
+ *          device (cudaGetSymbolAddress, which allocates nothing), so a
+ *          device reset cannot leave a stale address behind. The first call
+ *          on a device may load the library's device code: make it before
+ *          any stream capture.
  *   Sharing: every call on a device uses the same array. Each call clears
  *          what must start at zero on `stream`, but calls that overlap on the
  *          GPU (other streams, other threads) race on it and must be ordered
- *          by the caller. art_read_device_status cannot read this array.
+ *          by the caller. Its status word is read with art_read_static_status.
  */
 int art_decode_static(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_table, const int32_t* seq_lens,
                       const int32_t* visit_order, float eps_mag, float eps_dir,
                       int32_t patience, const int32_t* probe_idx, void* out,
                       int32_t* blocks_used, const art_shape* shape, void* stream);
+
+/* Copies the status word of art_decode_static's array on the current device
+ * (the ART_STATUS_* bits of the last call there; a blocking copy: call it
+ * after the stream has finished that call). An addition of this library; the
+ * ART paper has no counterpart. Returns ART_OK, ART_ERR_INVALID_ARG for a
+ * NULL `status`, or ART_ERR_LAUNCH. */
+int art_read_static_status(int32_t* status);
 
 /*
  * Key-based block selection: writes a visit list for art_decode (ART paper

@@ -22,7 +22,7 @@ ART_OK, ART_ERR_INVALID_ARG, ART_ERR_UNSUPPORTED, ART_ERR_WORKSPACE, ART_ERR_LAU
 STATUS_BITS = {1: "bad visit entry", 2: "duplicate visit entry", 4: "bad page id", 8: "bad seq_len",
                16: "bad probe index", 32: "wait timeout", 64: "internal check failed"}
 EXPORTS = ("art_workspace_bytes", "art_decode_path", "art_decode", "art_decode_ex", "dense_decode",
-           "art_decode_static", "art_read_device_status",
+           "art_decode_static", "art_read_static_status", "art_read_device_status",
            "art_status_string", "art_last_cuda_error", "art_set_timing_events",
            "art_select_workspace_bytes", "art_select_blocks")
 
@@ -75,6 +75,8 @@ def lib(path: str = LIB_PATH) -> ctypes.CDLL:
             L.art_decode_ex.restype = ctypes.c_int
             L.art_decode_static.argtypes = [P, P, P, P, P, P, F32, F32, I32, P, P, P, SP, P]
             L.art_decode_static.restype = ctypes.c_int
+            L.art_read_static_status.argtypes = [ctypes.POINTER(I32)]
+            L.art_read_static_status.restype = ctypes.c_int
             L.art_set_timing_events.argtypes = [P, P]
             L.art_set_timing_events.restype = None
             L.art_select_workspace_bytes.argtypes = [SP]
@@ -206,6 +208,13 @@ def set_timing_events(start=None, stop=None):
     no arguments clears."""
     h = lambda e: None if e is None else ctypes.c_void_p(int(e.cuda_event))
     lib().art_set_timing_events(h(start), h(stop))
+
+
+def art_read_static_status() -> int:
+    """Status word of art_decode_static's array on the current device (blocking)."""
+    st = ctypes.c_int32(0)
+    _check(lib().art_read_static_status(ctypes.byref(st)))
+    return int(st.value)
 
 
 def art_read_device_status(workspace) -> int:

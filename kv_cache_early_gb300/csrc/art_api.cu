@@ -3,7 +3,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
+#include <cstddef>
 #include <string>
 
 #include "art_units.cuh"
@@ -30,6 +30,7 @@ struct PlanParams {
     // ctas = CTAs of the unit kernel (sets the unit length), patience = the call's;
     // dense = the full-scan twin (every item stops at its last block, no fix pieces)
     int units, maxk, ctas, patience, dense;
+    int ck_force;  // unit length forced by ART_CK (0: chosen here)
     int* p0;
     int* stop_min;
     int* resolved;
@@ -80,7 +81,6 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams p) {
     __shared__ unsigned int bitmap[kBitmapWords];
     __shared__ int s_hist[kSortBuckets];
-    __shared__ int s_part[kPlanThreads];
     __shared__ long long s_warp[kPlanThreads / 32];
     __shared__ int s_n, s_flags, s_last, s_p0;
     const int item = blockIdx.x, tid = threadIdx.x;
@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
             const long long waves = total > 0 ? (total + cap - 1) / cap : 1;
             long long ck = (total + waves * p.ctas - 1) / (waves * p.ctas);
             ck = ck < kUnitMinBlocks ? kUnitMinBlocks : ck > kUnitBlocks ? kUnitBlocks : ck;
+            if (p.ck_force) ck = p.ck_force;
             if (ck < p.patience) ck = p.patience;
             s_ck = (int)ck;
             p.hdr->ck = (int)ck;
@@ -226,50 +227,58 @@ __global__ void __launch_bounds__(kPlanThreads) art_plan_kernel(const PlanParams
         p.order[pos] = it;
     }
     if (!p.units) return;
-    // unit path (num_items <= kPlanThreads): thread o holds claim position o
+    // unit path: cnt_k = items with more than k units (a prefix of the claim order, which
+    // is by units, descending), S_k = units numbered before round k; unit k of the item
+    // at claim position o gets number S_k + o
     __syncthreads();
-    int* s_nch = s_part;
-    const int o = tid;
-    const int my_item = o < p.num_items ? __ldcg(&p.order[o]) : -1;
-    const int my_nch = o < p.num_items ? sort_key(my_item) : 0;
-    s_nch[o] = my_nch;
+    for (int i = tid; i < kSortBuckets; i += kPlanThreads) s_hist[i] = 0;
     __syncthreads();
-    const int kmax = s_nch[0];  // units of the longest list (the order is by units, descending)
-    // cnt_k = items with more than k units = the first position whose item has <= k units
-    for (int k = tid; k < kmax; k += kPlanThreads) {
-        int lo = 0, hi = p.num_items;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (s_nch[mid] > k) lo = mid + 1; else hi = mid;
+    for (int it = tid; it < p.num_items; it += kPlanThreads) {
+        const int nn = sort_key(it);  // <= maxk < kUnitMaxK = kSortBuckets
+        if (nn > 0) atomicAdd(&s_hist[nn - 1], 1);
+    }
+    __syncthreads();
+    // items with at most k units = exclusive prefix P_k of the histogram; cnt_k = items - P_k
+    {
+        int csum = 0;
+        for (int i = 0; i < per; ++i) csum += s_hist[tid * per + i];
+        long long tot = 0;
+        int run2 = (int)block_exclusive_scan(csum, s_warp, tot);
+        const int with_units = (int)tot;
+        for (int i = 0; i < per; ++i) {
+            const int k = tid * per + i;
+            const int hk = s_hist[k];
+            s_hist[k] = with_units - run2;  // cnt_k
+            run2 += hk;
         }
-        s_hist[k] = lo;
     }
     __syncthreads();
-    // S_k = units numbered before round k (exclusive prefix of cnt over 0 .. kmax - 1)
-    int chunk_sum = 0;
-    for (int i = 0; i < per; ++i) {
-        const int k = tid * per + i;
-        chunk_sum += k < kmax ? s_hist[k] : 0;
+    {
+        int csum = 0;
+        for (int i = 0; i < per; ++i) csum += s_hist[tid * per + i];
+        long long n_reg = 0;
+        int acc = (int)block_exclusive_scan(csum, s_warp, n_reg);
+        if (tid == 0) {
+            p.hdr->n_regular = (int)n_reg;
+            p.hdr->n_units = (int)n_reg + (p.dense ? 0 : p.num_items * s_ck);  // then ck fix pieces per item
+        }
+        for (int i = 0; i < per; ++i) {
+            const int k = tid * per + i;
+            const int t = s_hist[k];
+            s_hist[k] = acc;  // S_k
+            acc += t;
+        }
     }
     __syncthreads();
-    long long n_reg = 0;
-    int acc = (int)block_exclusive_scan(chunk_sum, s_warp, n_reg);
-    if (tid == 0) {
-        p.hdr->n_regular = (int)n_reg;
-        p.hdr->n_units = (int)n_reg + (p.dense ? 0 : p.num_items * s_ck);  // then ck fix pieces per item
-    }
-    for (int i = 0; i < per; ++i) {
-        const int k = tid * per + i;
-        const int t = k < kmax ? s_hist[k] : 0;
-        s_hist[k] = acc;
-        acc += t;
-    }
-    __syncthreads();
-    for (int k = 0; k < my_nch; ++k) p.ulist[s_hist[k] + o] = make_int2(my_item, k);
-    if (p.dense && my_item >= 0 && my_nch > 0) {
-        // the twin reads every listed block: each item stops at its last one
-        p.stop_min[my_item] = __ldcg(reinterpret_cast<const int*>(&p.info[my_item])) - 1;
-        p.resolved[my_item] = my_nch;
+    for (int o = tid; o < p.num_items; o += kPlanThreads) {
+        const int my_item = __ldcg(&p.order[o]);
+        const int my_nch = sort_key(my_item);
+        for (int k = 0; k < my_nch; ++k) p.ulist[s_hist[k] + o] = make_int2(my_item, k);
+        if (p.dense && my_nch > 0) {
+            // the twin reads every listed block: each item stops at its last one
+            p.stop_min[my_item] = __ldcg(reinterpret_cast<const int*>(&p.info[my_item])) - 1;
+            p.resolved[my_item] = my_nch;
+        }
     }
 }
 
@@ -338,26 +347,26 @@ static cudaError_t dispatch_units(const art_shape& s, const Params& p, const UPa
     return cudaErrorInvalidValue;
 }
 
-// The unit path (one item spread over many CTAs) is offered for bf16 with up to
-// kUnitMaxItems items; its workspace area is sized for the longest list the
-// block table allows.
+// The unit path (one item spread over many CTAs) is offered for bf16 when its
+// workspace area, sized for the longest list the block table allows, stays within
+// kUnitMaxWsBytes.
 static int unit_maxk(const art_shape& s) {
     const long long tmax = ((long long)s.max_pages_per_seq * s.page_size + kBK - 1) / kBK;
     const long long k = (tmax + kUnitMinBlocks - 1) / kUnitMinBlocks;
     return k > kUnitMaxK ? 0 : (int)k;
 }
 
+static size_t unit_bytes(const art_shape& s) {
+    const int items = s.batch * s.num_kv_heads;
+    return make_unit_ws(items, unit_maxk(s), s.head_dim, s.num_q_heads / s.num_kv_heads).total;
+}
+
 static bool unit_eligible(const art_shape& s) {
-    const long long items = (long long)s.batch * s.num_kv_heads;
-    return s.dtype == ART_DTYPE_BF16 && items <= kUnitMaxItems && unit_maxk(s) >= 1 && unit_maxk(s) < kUnitMaxK;
+    return s.dtype == ART_DTYPE_BF16 && unit_maxk(s) >= 1 && unit_maxk(s) < kUnitMaxK &&
+           unit_bytes(s) <= kUnitMaxWsBytes;
 }
 
 static size_t unit_area_offset(int num_items) { return align_up(workspace_bytes_for(num_items), 256); }
-
-static size_t unit_bytes(const art_shape& s) {
-    const int items = s.batch * s.num_kv_heads;
-    return make_unit_ws(items, unit_maxk(s), s.head_dim).total;
-}
 
 // Unit path or one CTA per item: ART_UNITS=0/1 forces the choice (where the
 // path is offered); otherwise the unit path runs when there are fewer items
@@ -416,7 +425,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     std::memset(&up, 0, sizeof up);
     if (units) {
         unsigned char* base = static_cast<unsigned char*>(workspace) + unit_area_offset(num_items);
-        const UnitWs w = make_unit_ws(num_items, unit_maxk(s), s.head_dim);
+        const UnitWs w = make_unit_ws(num_items, unit_maxk(s), s.head_dim, s.num_q_heads / s.num_kv_heads);
         up.ulist = reinterpret_cast<const int2*>(base + w.ulist);
         up.p0 = reinterpret_cast<const int*>(base + w.p0);
         up.stop_min = reinterpret_cast<int*>(base + w.stop_min);
@@ -457,6 +466,11 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     pp.patience = kART ? patience : 1;
     pp.dense = kART ? 0 : 1;
     pp.ctas = 0;
+    pp.ck_force = 0;
+    if (const char* eck = std::getenv("ART_CK")) {
+        const int v = std::atoi(eck);
+        if (v >= kUnitMinBlocks && v <= kUnitBlocks) pp.ck_force = v;
+    }
     if (units) {
         int dev = 0, sms = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
@@ -502,6 +516,17 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     p.patience = patience;
     p.ph = probe_heads > 0 ? probe_heads : s.num_q_heads / s.num_kv_heads;
     p.tma3d = 0;
+    // ART_TEST_STALL_NS=<ns> (tests of the failure path only): the consumer warps wait
+    // on a barrier that nothing completes, and every bounded wait gives up after <ns>
+    p.wait_ns = kWaitLimitNs;
+    p.stall = 0;
+    if (const char* es = std::getenv("ART_TEST_STALL_NS")) {
+        const long long ns = std::atoll(es);
+        if (ns > 0) {
+            p.stall = 1;
+            p.wait_ns = (unsigned long long)(ns < (long long)kWaitLimitNs ? ns : (long long)kWaitLimitNs);
+        }
+    }
     if (t_events.start && (e = cudaEventRecord(t_events.start, st)) != cudaSuccess) return cuda_fail(e);
     e = units ? dispatch_units<kART>(s, p, up, st, li) : dispatch<kART>(s, p, st, env_stages(), li);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -598,26 +623,15 @@ constexpr size_t kStaticWorkspaceBytes =
 // comes from cudaGetSymbolAddress (below).
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-constexpr int kStaticMaxDevices = 256;
-static void* g_static_workspace_addr[kStaticMaxDevices];
-static std::mutex g_static_mutex;
-
-// Device address of g_static_workspace on the current device; looked up once
-// per device, on that device's first call.
+// Device address of g_static_workspace on the current device, looked up on every
+// call: the lookup allocates nothing, and an address kept from an earlier call could
+// be stale after the device's context was reset and the module loaded again.
 static int static_workspace(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= kStaticMaxDevices) return ART_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_static_mutex);
-    if (!g_static_workspace_addr[dev]) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_static_workspace);
-        if (e != cudaSuccess) return cuda_fail(e);
-        if (!ptr) return ART_ERR_LAUNCH;
-        g_static_workspace_addr[dev] = ptr;
-    }
-    *out = g_static_workspace_addr[dev];
+    if (!ptr) return ART_ERR_LAUNCH;
+    *out = ptr;
     return ART_OK;
 }
 
@@ -635,4 +649,12 @@ extern "C" int art_decode_static(const void* q, const void* k_cache, const void*
     if (rs != ART_OK) return rs;
     return run<true>(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience, probe_idx,
                      out, blocks_used, shape, ws, kStaticWorkspaceBytes, stream, nullptr);
+}
+
+extern "C" int art_read_static_status(int32_t* status) {
+    if (!status) return ART_ERR_INVALID_ARG;
+    const cudaError_t e =
+        cudaMemcpyFromSymbol(status, art::g_static_workspace, sizeof(int32_t), offsetof(art::WsHeader, status));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ART_OK;
 }

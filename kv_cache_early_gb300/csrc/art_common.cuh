@@ -76,6 +76,13 @@ struct Params {
     float eps_mag, eps_dir;
     int patience;
     int ph;  // query heads 0 .. ph-1 of a group form the probe
+    // Bounded waits give up after wait_ns (kWaitLimitNs unless the test hook below is
+    // set); a producer's final drain of its own copies always allows kWaitLimitNs.
+    unsigned long long wait_ns;
+    // Test hook of the failure path: the consumer warps first wait on a barrier that
+    // nothing completes, so every warp of the CTA gives up at one of its bounded waits
+    // (none reaches a named barrier) and the call ends with ART_STATUS_TIMEOUT.
+    int stall;
 };
 
 // Launch geometry chosen for one call.

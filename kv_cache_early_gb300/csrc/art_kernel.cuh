@@ -39,11 +39,12 @@
 // change as delta.(2x + delta) / (|x_i| + |x_{i-1}|), and 1 - cos as
 // |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2.
 //
-// Every mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel sets
-// ART_STATUS_TIMEOUT, the producer waits for its own copies in flight, and
-// the CTA returns.
+// Every mbarrier wait is bounded (Params::wait_ns, 1 s); on expiry the kernel
+// sets ART_STATUS_TIMEOUT, the producer waits for its own copies in flight,
+// and the CTA returns.
 #pragma once
 
+#include <cstddef>
 #include <cstdlib>
 #include <cstring>
 
@@ -61,7 +62,9 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 
 enum Decision : int { kContinue = 0, kStop = 1, kDiscard = 2 };
 
-template <bool kBF16, int D, int G, int kNG = 1>
+// kSplitDims: one group of four tensor-core warps with the head dims split (the unit
+// kernel's consumers); otherwise three or four groups split the dims, one or two the keys
+template <bool kBF16, int D, int G, int kNG = 1, bool kSplitDims = false>
 struct Cfg {
     using E = Elem<kBF16>;
     static constexpr bool TC = kBF16;            // bf16: tensor-core consumers on swizzled tiles
@@ -74,7 +77,7 @@ struct Cfg {
     static constexpr int NB = TC ? 3 * NG : 2;
     // four tensor-core groups split the head dims between the warps of a group
     // (fewer registers per warp); one or two groups, and the fp32 warps, split the keys
-    static constexpr bool DS = TC && NG >= 3;
+    static constexpr bool DS = TC && (NG >= 3 || kSplitDims);
     // rows of block partials per record: with the dims split each probe column has
     // one writer; with the keys split, one row set per warp
     static constexpr int RGW = DS ? 1 : GW;
@@ -132,9 +135,10 @@ struct Ctrl {
     int dec[kMaxNB];
     int stop_item;
     int abort;
-    int pad0, pad1;
+    unsigned long long wait_ns;  // limit of the bounded waits (Params::wait_ns)
     SlotMeta info[kMaxNB];  // item and position of each published record
 };
+static_assert(offsetof(Ctrl, wait_ns) % 8 == 0, "8-byte field");
 
 struct Layout {
     size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, xb, sh, ptab, ctrl, total;
@@ -149,7 +153,7 @@ __host__ __device__ inline Layout make_layout(int stages) {
     o += (size_t)stages * sizeof(SlotMeta);
     o = align_up(o, 16);
     L.bars = o;
-    o += (size_t)(2 * stages + 2 * C::NB + 1) * sizeof(uint64_t);
+    o += (size_t)(2 * stages + 2 * C::NB + 2) * sizeof(uint64_t);  // ... cbar, then the stall barrier
     o = align_up(o, 16);
     L.part = o;  // [NB][RGW][PRW][PST] probe partial rows
     o += (size_t)C::PART_F * sizeof(float);
@@ -221,7 +225,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // hardware's own short time limit). Measured: the hint is 0.5 % faster with one
 // CTA per SM running three or four consumer groups, plain try_wait 2-3 % faster
 // with two CTAs per SM. Returns false (and sets ART_STATUS_TIMEOUT) when the wait
-// exceeds kWaitLimitNs. Only a warp's own wait ends it: the warps of a consumer
+// exceeds the CTA's limit (Ctrl::wait_ns). Only a warp's own wait ends it: the warps of a consumer
 // group always wait on the same barrier phases, so they give up together and
 // none is left behind in a named barrier.
 template <bool kHint = false>
@@ -237,7 +241,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctr
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (__all_sync(0xffffffffu, try_once())) return true;
-        int late = (threadIdx.x & 31) == 0 && global_ns() - t0 > kWaitLimitNs;
+        int late = (threadIdx.x & 31) == 0 && global_ns() - t0 > ctrl->wait_ns;
         if (__any_sync(0xffffffffu, late)) {
             if ((threadIdx.x & 31) == 0) {
                 st_volatile_shared(&ctrl->abort, 1);
@@ -1928,6 +1932,7 @@ __global__ void __launch_bounds__(Cfg<kBF16, D, G, kNG>::THREADS, (MinBlocks<Cfg
     uint64_t* part_full = empty + p.stages;
     uint64_t* dec_bar = part_full + C::NB;
     uint64_t* cbar = dec_bar + C::NB;
+    uint64_t* stall_bar = cbar + 1;  // never completed (the failure-path test hook)
     int* pmask = reinterpret_cast<int*>(smem + L.ptab);
     int* pbase = pmask + C::LPR;
     int* prank = pbase + C::LPR;
@@ -1945,8 +1950,10 @@ __global__ void __launch_bounds__(Cfg<kBF16, D, G, kNG>::THREADS, (MinBlocks<Cfg
             ctrl->dec[b] = 0;
         }
         mbar_init(cbar, NWC);
+        mbar_init(stall_bar, 1);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
+        ctrl->wait_ns = p.wait_ns;
         fence_mbar_init();
     }
     if (tid < C::LPR) {
@@ -1983,6 +1990,7 @@ __global__ void __launch_bounds__(Cfg<kBF16, D, G, kNG>::THREADS, (MinBlocks<Cfg
     __syncthreads();
 
     const int warp = tid >> 5;
+    if (p.stall && warp < NWC && !wait_bounded(stall_bar, 0u, ctrl, p.hdr, 161)) return;
     if (warp == NWC) {
         producer_warp<C, kART>(p, ring, meta, full, empty, ctrl, &tk, &tv);
     } else if (warp == NWC + 1) {

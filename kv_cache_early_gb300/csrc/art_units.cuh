@@ -60,7 +60,7 @@ namespace art {
 constexpr int kUnitBlocks = 16;     // ck: ART blocks per unit at most
 constexpr int kUnitMinBlocks = 8;   // ... and at least (the workspace is sized for it)
 constexpr int kUnitRecs = 4;        // block records in flight from the consumers to the statistics warp
-constexpr int kUnitMaxItems = 256;  // the unit path is offered up to this many items
+constexpr size_t kUnitMaxWsBytes = (size_t)4 << 30;  // the unit path's workspace area at most
 constexpr int kUnitMaxK = 4096;     // units per item at most
 constexpr int kUnitWords = 10;      // words per lane of a probe state: max, weight sum, 8 probe slots
 
@@ -85,7 +85,12 @@ struct UnitWs {
     size_t p0, stop_min, resolved, fail, ulist, tflag, uflags, agg, incl, part_o, part_ml, fix_o, fix_ml, total;
 };
 
-__host__ __device__ inline UnitWs make_unit_ws(int items, int maxk, int D) {
+// Partials are merged over the CTA's warps before they are written: per unit (and per
+// fix piece) G*D output sums [head][dim], then 16 words: the max of each head (words
+// 0..7) and its weight sum (words 8..15).
+constexpr int kUnitMlWords = 16;
+
+__host__ __device__ inline UnitWs make_unit_ws(int items, int maxk, int D, int G) {
     UnitWs w;
     const size_t U = (size_t)items * maxk;
     size_t o = 0;
@@ -103,10 +108,10 @@ __host__ __device__ inline UnitWs make_unit_ws(int items, int maxk, int D) {
     w.uflags = take(U * 16);
     w.agg = take(U * 32 * kUnitWords * 4);
     w.incl = take(U * 32 * kUnitWords * 4);
-    w.part_o = take(U * 32 * (size_t)D * 4);
-    w.part_ml = take(U * 64 * 4);
-    w.fix_o = take((size_t)items * kUnitBlocks * 32 * D * 4);
-    w.fix_ml = take((size_t)items * kUnitBlocks * 64 * 4);
+    w.part_o = take(U * (size_t)G * D * 4);
+    w.part_ml = take(U * kUnitMlWords * 4);
+    w.fix_o = take((size_t)items * kUnitBlocks * G * D * 4);
+    w.fix_ml = take((size_t)items * kUnitBlocks * kUnitMlWords * 4);
     w.total = o;
     return w;
 }
@@ -121,8 +126,8 @@ struct UParams {
     int* uflags;        // per (item, k): {stable bits, blocks, state (1 set, 3 skipped), 0}
     float* agg;         // per (item, k): [kUnitWords][32 lanes] probe state of the unit's blocks
     float* incl;        // per (item, k): the same through the unit (from the list's start)
-    float* part_o;      // per (item, k): [4 warps][32 lanes][D / 4] output sums (mma fragment order)
-    float* part_ml;     // per (item, k): [4 warps][2][8] running max, weight sum per head column
+    float* part_o;      // per (item, k): [G][D] output sums, merged over the warps
+    float* part_ml;     // per (item, k): max of each head (words 0..7), weight sum (words 8..15)
     float* fix_o;       // per (item, fix piece): the piece's partial, same layout
     float* fix_ml;
     int ck;             // ART blocks per unit (the kernels take it from the workspace header)
@@ -141,14 +146,14 @@ struct URec {
 
 template <int D, int G>
 struct UCfg {
-    using C = Cfg<true, D, G, 1>;
+    using C = Cfg<true, D, G, 1, true>;  // one group of four warps, head dims split
     static constexpr int THREADS = 7 * 32;  // 4 consumer warps, producer, block summaries, tests
     static constexpr int W = C::SPL + 2;
     static_assert(W <= kUnitWords, "probe state fits the workspace words");
 };
 
 struct ULayout {
-    size_t meta, bars, part, plb, pmb, qt, ptab, rinfo, ust, uhdr, uagg, ctrl, total;
+    size_t meta, bars, part, plb, pmb, qt, xb, ptab, rinfo, ust, uhdr, uagg, ctrl, total;
 };
 
 template <int D, int G>
@@ -160,17 +165,22 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)stages * sizeof(UMeta);
     o = align_up(o, 16);
     L.bars = o;  // full[stages], empty[stages], part_full[NB], part_empty[NB]
-    o += (size_t)(2 * stages + 2 * kUnitRecs + 2) * sizeof(uint64_t);  // ... then ufull, uempty
+    o += (size_t)(2 * stages + 2 * kUnitRecs + 3) * sizeof(uint64_t);  // ... then ufull, uempty, stall
     o = align_up(o, 16);
-    L.part = o;  // [NB][4 warps][PRW][PST] probe partial rows
-    o += (size_t)kUnitRecs * C::GW * C::PRW * C::PST * sizeof(float);
-    L.plb = o;  // [NB][4][G] block weight sums
-    o += (size_t)kUnitRecs * C::GW * G * sizeof(float);
-    L.pmb = o;  // [NB][4][G] block maxima
-    o += (size_t)kUnitRecs * C::GW * G * sizeof(float);
+    static_assert(C::DS && C::RGW == 1, "one writer per probe column");
+    L.part = o;  // [NB][PRW][PST] probe partial rows (one writer per column)
+    o += (size_t)kUnitRecs * C::PRW * C::PST * sizeof(float);
+    L.plb = o;  // [NB][G] block weight sums
+    o += (size_t)kUnitRecs * G * sizeof(float);
+    L.pmb = o;  // [NB][G] block maxima (integer exponents)
+    o += (size_t)kUnitRecs * G * sizeof(float);
     o = align_up(o, 1024);
-    L.qt = o;  // the unit's queries, 8 rows (heads past G zero), 128B-swizzled
-    o += (size_t)8 * C::ROWB;
+    L.qt = o;  // per consumer warp: the unit's queries, 8 rows (heads past G zero), 128B-swizzled
+    o += (size_t)C::GW * 8 * C::ROWB;
+    o = align_up(o, 16);
+    L.xb = o;  // [2 block parities][4 warps][32 lanes] P^T fragments, then [2][8][4] exponents,
+               // then [2][8][4] weight sums
+    o += (size_t)C::XGB;
     L.ptab = o;  // rank of each head dim among the probe dims, or -1
     o += (size_t)D * sizeof(int);
     o = align_up(o, 16);
@@ -186,7 +196,8 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)UCfg<D, G>::W * 32 * sizeof(float);
     o = align_up(o, 16);
     L.ctrl = o;  // only the abort and stop_item words of a Ctrl are used here
-    static_assert(offsetof(Ctrl, abort) + sizeof(int) <= 128 && offsetof(Ctrl, stop_item) + sizeof(int) <= 128,
+    static_assert(offsetof(Ctrl, abort) + sizeof(int) <= 128 && offsetof(Ctrl, stop_item) + sizeof(int) <= 128 &&
+                      offsetof(Ctrl, wait_ns) + sizeof(unsigned long long) <= 128,
                   "the words of Ctrl used by the unit kernel fit its 128 bytes");
     o += 128;
     L.total = align_up(o, 128) + 1024;  // room to align the ring to 1024 bytes
@@ -194,7 +205,7 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
 }
 
 // Polls a global flag until it is >= want (the value read goes to `got`);
-// false when this CTA gave up elsewhere or after kWaitLimitNs. Every lane
+// false when this CTA gave up elsewhere or after its wait limit. Every lane
 // then loads the flag once more with acquire semantics, so each lane's later
 // loads of the payload are ordered after it.
 __device__ __forceinline__ bool poll_flag(const int* flag, int want, int& got, Ctrl* ctrl, WsHeader* hdr,
@@ -213,7 +224,7 @@ __device__ __forceinline__ bool poll_flag(const int* flag, int want, int& got, C
         int quit = 0;
         if (lane == 0) {
             if (ld_volatile_shared(&ctrl->abort)) quit = 1;
-            else if ((it & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+            else if ((it & 63u) == 63u && global_ns() - t0 > ctrl->wait_ns) {
                 st_volatile_shared(&ctrl->abort, 1);
                 atomicOr(&hdr->status, ART_STATUS_TIMEOUT);
                 record_check(hdr, where, want, v, 0);
@@ -442,14 +453,29 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
 }
 
 // ---------------------------------------------------------------------------
-// consumer warps (one group of 4; warp wg owns keys 16 wg .. 16 wg + 15 of a block)
+// consumer warps: one group of four, head dims split between them.
+//
+// Warp wg computes the scores of keys 16 wg .. 16 wg + 15 of a block (S^T = K Q^T
+// with mma.m16n8k16 from the swizzled tiles) and their weights p = 2^(s - e)
+// against its own max rounded up to an integer exponent e. The four warps
+// exchange the P^T fragments, exponents and weight sums through shared memory
+// (one named barrier per block); warp wg then computes O^T for head dims
+// wg D/4 .. (wg + 1) D/4 - 1 over all 64 keys, each key chunk's fragment scaled to
+// the block's largest exponent exactly (a bf16 multiply by a power of two). The
+// weights enter P.V as bf16 high + low parts (for G <= 4 both share one 8-column
+// tile). Every warp so holds the same block max and weight sum per head, and each
+// probe column has one writer. The block is folded into the unit's running state
+// at once (no decision is waited for); at the unit's last block each warp writes
+// its own dims of the unit's partial.
 // ---------------------------------------------------------------------------
 template <class C, bool kART>
 __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ring, const UMeta* meta,
                            uint64_t* full, uint64_t* empty, uint64_t* part_full, uint64_t* part_empty, URec* rinfo,
                            const ULayout& L, unsigned char* smem, const int* prank, Ctrl* ctrl) {
     constexpr int G = C::GQ, D = C::DD, KS = C::KS, GW = C::GW, NB = kUnitRecs;
+    constexpr int DW = C::DW, MT = C::MT, XBW = C::XBW;
     constexpr bool SPLITN = C::SPLITN;
+    static_assert(C::DS && GW == 4, "four warps, head dims split");
     const int wg = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane >> 2, tig = lane & 3;
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
@@ -460,33 +486,38 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
     const int q0 = lo_lane ? h0 - 4 : h0, q1 = q0 + 1;
     const bool u0 = q0 < G, u1 = q1 < G;
     const bool w0 = u0 && !lo_lane, w1 = u1 && !lo_lane;
-    float* part = reinterpret_cast<float*>(smem + L.part);
+    const int hb = (SPLITN && grp >= 4) ? grp - 4 : grp;  // the head of this lane's P^T fragment column
     float* plb = reinterpret_cast<float*>(smem + L.plb);
     float* pmb = reinterpret_cast<float*>(smem + L.pmb);
-    unsigned char* sQt = smem + L.qt;
+    uint32_t* xb = reinterpret_cast<uint32_t*>(smem + L.xb);
+    float* xm = reinterpret_cast<float*>(xb + 2 * GW * 32 * XBW);
+    float* xl = xm + 2 * 8 * GW;
+    unsigned char* sQt = smem + L.qt + (size_t)wg * 8 * C::ROWB;  // this warp's copy of the unit's queries
     const uint32_t qtbase = smem_addr(sQt);
     const float scale = 1.4426950408889634f / sqrtf((float)D);
-    const int gtid = threadIdx.x;  // 0 .. 127
-    // this lane's O^T rows are d = 16 mt + grp + 8 r; bit 2 mt + r marks a probe dim,
-    // byte 2 mt + r of prk holds its rank among the probe dims
+    // this lane's O^T rows are d = wg DW + 16 mt + 8 r + grp; bit 2 mt + r marks a probe
+    // dim, pofs[2 mt + r] the byte offset of its slot in a record's partial rows
     uint32_t pbits = 0;
-    uint32_t prk[(2 * KS + 3) / 4];
+    uint32_t pofs[2 * MT];
 #pragma unroll
-    for (int i = 0; i < (2 * KS + 3) / 4; ++i) prk[i] = 0;
+    for (int k = 0; k < 2 * MT; ++k) pofs[k] = 0;
+    if (kART) {
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int rk = prank[16 * mt + grp + 8 * r];
-            if (rk >= 0) {
-                pbits |= 1u << (2 * mt + r);
-                prk[(2 * mt + r) >> 2] |= (uint32_t)rk << (8 * ((2 * mt + r) & 3));
+            for (int r = 0; r < 2; ++r) {
+                const int rk = prank[wg * DW + 16 * mt + 8 * r + grp];
+                if (rk >= 0 && u0) {
+                    pbits |= 1u << (2 * mt + r);
+                    pofs[2 * mt + r] = (uint32_t)(((lo_lane ? C::PST : 0) + q0 + rk * C::GP) * 4);
+                }
             }
-        }
+    }
+    const uint32_t part_base = smem_addr(smem + L.part);
     const int mi = lane >> 3, lr = lane & 7;
-    const int keyK = wg * 16 + (mi & 1) * 8 + lr;   // K rows for the S^T A fragments
+    const int keyK = wg * 16 + (mi & 1) * 8 + lr;  // K rows for the S^T A fragments
     const int chK = mi >> 1;
-    const int keyV = wg * 16 + (mi >> 1) * 8 + lr;  // V rows for the O^T A fragments
+    const int keyV = (mi >> 1) * 8 + lr;  // V rows (within a 16-key chunk) for the O^T A fragments
     const int chV = mi & 1;
     const int PR = p.Ps < kBK ? p.Ps : kBK;
     const int lpr = 31 - __clz(PR);
@@ -497,7 +528,7 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
         return base + rowoff(row) + (uint32_t)((chunk >> 3) * PR * 128 + (((chunk & 7) ^ (row & 7)) << 4));
     };
 
-    float acc[KS][4], tN[KS][4];
+    float acc[MT][4], tN[MT][4];
     float mrun[2], lrun[2], mbN[2], lbN[2];
     auto reset = [&]() {
 #pragma unroll
@@ -506,7 +537,7 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
             lrun[j] = 0.f;
         }
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
     };
@@ -524,31 +555,31 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
             mrun[j] = mn;
         }
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[mt][c] = a[c & 1] * acc[mt][c] + bb[c & 1] * tN[mt][c];
     };
-    int rec = 0;  // records published to the statistics warp
+    int rec = 0;  // records published to the summary warp
     auto publish = [&](const UMeta& mt, int kind, bool data) -> bool {
         const int rb = rec % NB;
         if (rec >= NB && !wait_bounded(&part_empty[rb], (uint32_t)(rec / NB - 1) & 1u, ctrl, p.hdr, 242))
             return false;
         if (data) {
-            float* pp = part + (((size_t)rb * GW + wg) * C::PRW + (lo_lane ? 1 : 0)) * C::PST + q0;
+            // probe partial rows (high and low parts with the split tile); predicated stores
+            const uint32_t rp = part_base + (uint32_t)(rb * C::PRW * C::PST * 4);
 #pragma unroll
-            for (int m = 0; m < KS; ++m)
+            for (int m = 0; m < MT; ++m)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const bool on = (pbits >> (2 * m + r)) & 1u;
-                    const int rank = (int)((prk[(2 * m + r) >> 2] >> (8 * ((2 * m + r) & 3))) & 0xffu);
-                    float* dst = pp + rank * C::GP;
-                    if (G >= 2) st_shared_if(on && u1, dst, tN[m][2 * r], tN[m][2 * r + 1]);
-                    if (G % 2) st_shared_if(on && u0 && !u1, dst, tN[m][2 * r]);
+                    if (G >= 2) st_shared_if(on && u1, rp + pofs[2 * m + r], tN[m][2 * r], tN[m][2 * r + 1]);
+                    if (G % 2) st_shared_if(on && !u1, rp + pofs[2 * m + r], tN[m][2 * r]);
                 }
-            st_shared_if(grp == 0 && w0, &plb[(rb * GW + wg) * G + (w0 ? q0 : 0)], lbN[0]);
-            st_shared_if(grp == 0 && w1, &plb[(rb * GW + wg) * G + (w1 ? q1 : 0)], lbN[1]);
-            st_shared_if(grp == 0 && w0, &pmb[(rb * GW + wg) * G + (w0 ? q0 : 0)], mbN[0]);
-            st_shared_if(grp == 0 && w1, &pmb[(rb * GW + wg) * G + (w1 ? q1 : 0)], mbN[1]);
+            const bool lead = wg == 0 && grp == 0;
+            st_shared_if(lead && w0, &plb[rb * G + (w0 ? q0 : 0)], lbN[0]);
+            st_shared_if(lead && w1, &plb[rb * G + (w1 ? q1 : 0)], lbN[1]);
+            st_shared_if(lead && w0, &pmb[rb * G + (w0 ? q0 : 0)], mbN[0]);
+            st_shared_if(lead && w1, &pmb[rb * G + (w1 ? q1 : 0)], mbN[1]);
         }
         if (wg == 0 && lane == 0) {
             URec& r = rinfo[rb];
@@ -559,41 +590,55 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
         ++rec;
         return true;
     };
-    // the unit's partial: output sums in mma fragment order, then max and weight sum per head
+    // the unit's partial: this warp's dims of the [G][D] output sums; every warp holds
+    // the same running max and weight sum, which warp 0 writes
     auto write_partial = [&](const UMeta& mt) {
         float* po;
         float* pml;
         if (mt.kind == kUFix) {
             const size_t ip = (size_t)mt.item * up.ck + mt.k;
-            po = up.fix_o + ip * 32 * D;
-            pml = up.fix_ml + ip * 64;
+            po = up.fix_o + ip * G * D;
+            pml = up.fix_ml + ip * kUnitMlWords;
         } else {
             const size_t iu = (size_t)mt.item * up.maxk + mt.k;
-            po = up.part_o + iu * 32 * D;
-            pml = up.part_ml + iu * 64;
+            po = up.part_o + iu * G * D;
+            pml = up.part_ml + iu * kUnitMlWords;
         }
         if constexpr (SPLITN) {
             // high + low parts (both lanes carry the same running max and sum)
 #pragma unroll
-            for (int m = 0; m < KS; ++m)
+            for (int m = 0; m < MT; ++m)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[m][c] += __shfl_xor_sync(0xffffffffu, acc[m][c], 2);
         }
-        float4* dst = reinterpret_cast<float4*>(po + ((size_t)wg * 32 + lane) * (KS * 4));
 #pragma unroll
-        for (int m = 0; m < KS; ++m) dst[m] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-        if (grp == 0) {
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int d = wg * DW + 16 * m + 8 * r + grp;
+                if (w0) po[q0 * D + d] = acc[m][2 * r];
+                if (w1) po[q1 * D + d] = acc[m][2 * r + 1];
+            }
+        if (wg == 0 && grp == 0) {
             if (w0) {
-                pml[wg * 16 + q0] = mrun[0];
-                pml[wg * 16 + 8 + q0] = lrun[0];
+                pml[q0] = mrun[0];
+                pml[8 + q0] = lrun[0];
             }
             if (w1) {
-                pml[wg * 16 + q1] = mrun[1];
-                pml[wg * 16 + 8 + q1] = lrun[1];
+                pml[q1] = mrun[1];
+                pml[8 + q1] = lrun[1];
             }
         }
     };
+    // bf16x2 multiplier 2^(e - emax) for a power-of-two exponent difference (0 below bf16 range)
+    auto pow2_bf16x2 = [](float e, float emax) -> uint32_t {
+        const float d = e - emax;  // an integer <= 0, or NaN / -inf
+        const int k = d >= -126.f ? (int)d : -1000;
+        const uint32_t bits = k >= -126 ? (uint32_t)(k + 127) << 7 : 0u;
+        return bits | (bits << 16);
+    };
 
+    int xpar = 0;  // exchange buffer of the next block
     for (int e = 0;; ++e) {
         const int slot = e % p.stages;
         if (!wait_bounded(&full[slot], (uint32_t)(e / p.stages) & 1u, ctrl, p.hdr, 241)) return;
@@ -614,19 +659,18 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
         unsigned char* sK = ring + (size_t)slot * C::SLOT;
         unsigned char* sV = sK + C::KVB;
         if (mt.j == 0) {
-            // the unit's queries into the swizzled 8-row area (rows past G zero), once every
-            // warp has finished the previous block's scores
+            // the unit's queries into this warp's own swizzled 8-row area (rows past G zero)
             reset();
-            named_bar_sync(1, GW * 32);
             const unsigned char* sQ = sK + 2 * C::KVB;
             constexpr int QCH = 8 * (C::ROWB / 16);
-            for (int i = gtid; i < QCH; i += GW * 32) {
+#pragma unroll
+            for (int i = lane; i < QCH; i += 32) {
                 const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
                 const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
                                           : make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
             }
-            named_bar_sync(1, GW * 32);
+            __syncwarp();
         }
         const int nvalid = mt.nvalid;
         // ---- S^T for this warp's 16 keys (two independent accumulation chains)
@@ -656,81 +700,125 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
         sc[1] = (k0 < nvalid && v1) ? s4[1] * scale : -INFINITY;
         sc[2] = (k1 < nvalid && v0) ? s4[2] * scale : -INFINITY;
         sc[3] = (k1 < nvalid && v1) ? s4[3] * scale : -INFINITY;
-        // ---- this warp's block max per head (each warp keeps its own running max)
-        float mb0 = fmaxf(sc[0], sc[2]), mb1 = fmaxf(sc[1], sc[3]);
+        // ---- this warp's max per head over its keys, rounded up to an integer exponent
+        float e0 = fmaxf(sc[0], sc[2]), e1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
-            mb0 = fmaxf(mb0, __shfl_xor_sync(0xffffffffu, mb0, o));
-            mb1 = fmaxf(mb1, __shfl_xor_sync(0xffffffffu, mb1, o));
+            e0 = fmaxf(e0, __shfl_xor_sync(0xffffffffu, e0, o));
+            e1 = fmaxf(e1, __shfl_xor_sync(0xffffffffu, e1, o));
         }
+        e0 = ceilf(e0);
+        e1 = ceilf(e1);
         float pw[4];
-        pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mb0);
-        pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mb1);
-        pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - mb0);
-        pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - mb1);
+        pw[0] = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - e0);
+        pw[1] = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - e1);
+        pw[2] = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - e0);
+        pw[3] = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - e1);
         float l0 = pw[0] + pw[2], l1 = pw[1] + pw[3];
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, o);
             l1 += __shfl_xor_sync(0xffffffffu, l1, o);
         }
-        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        // ---- P^T fragments of this warp's keys: hi and lo bf16 parts, transposed by movmatrix
+        uint32_t bf[XBW];
         if constexpr (SPLITN) {
-            // low-part lanes take the weights, maxima and sums of lane ^ 2
+            // low-part lanes take the weights of lane ^ 2
             float px[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) px[c] = __shfl_xor_sync(0xffffffffu, pw[c], 2);
-            const float mx0 = __shfl_xor_sync(0xffffffffu, mb0, 2), mx1 = __shfl_xor_sync(0xffffffffu, mb1, 2);
-            const float lx0 = __shfl_xor_sync(0xffffffffu, l0, 2), lx1 = __shfl_xor_sync(0xffffffffu, l1, 2);
             float t[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) t[c] = lo_lane ? px[c] : pw[c];
-            mbN[0] = lo_lane ? mx0 : mb0;
-            mbN[1] = lo_lane ? mx1 : mb1;
-            lbN[0] = lo_lane ? lx0 : l0;
-            lbN[1] = lo_lane ? lx1 : l1;
             const uint32_t hA = pack_bf16(t[0], t[1]), hB = pack_bf16(t[2], t[3]);
             const uint32_t lA = pack_bf16(t[0] - bf16_lo_f(hA), t[1] - bf16_hi_f(hA));
             const uint32_t lB = pack_bf16(t[2] - bf16_lo_f(hB), t[3] - bf16_hi_f(hB));
             __syncwarp();
-            bh0 = movm_t(lo_lane ? lA : hA);
-            bh1 = movm_t(lo_lane ? lB : hB);
+            bf[0] = movm_t(lo_lane ? lA : hA);
+            bf[1] = movm_t(lo_lane ? lB : hB);
         } else {
-            mbN[0] = mb0;
-            mbN[1] = mb1;
-            lbN[0] = l0;
-            lbN[1] = l1;
             const uint32_t hA = pack_bf16(pw[0], pw[1]), hB = pack_bf16(pw[2], pw[3]);
             const uint32_t lA = pack_bf16(pw[0] - bf16_lo_f(hA), pw[1] - bf16_hi_f(hA));
             const uint32_t lB = pack_bf16(pw[2] - bf16_lo_f(hB), pw[3] - bf16_hi_f(hB));
             __syncwarp();
-            bh0 = movm_t(hA);
-            bh1 = movm_t(hB);
-            bl0 = movm_t(lA);
-            bl1 = movm_t(lB);
+            bf[0] = movm_t(hA); bf[1] = movm_t(hB); bf[2] = movm_t(lA); bf[3] = movm_t(lB);
         }
-        // ---- rows past the sequence end hold stale data: zero this warp's, so 0 * V stays 0
-        if (nvalid < wg * 16 + 16) {
-            const int r0 = max(nvalid, wg * 16);
-            const int nchunks = (wg * 16 + 16 - r0) * (C::ROWB / 16);
+        // ---- publish fragments, exponents and sums to the group (every head column,
+        // -inf / 0 for heads past G), then wait for the other warps
+        uint32_t* xbp = xb + (size_t)xpar * GW * 32 * XBW;
+        float* xmp = xm + xpar * 8 * GW;
+        float* xlp = xl + xpar * 8 * GW;
+        if constexpr (XBW == 2)
+            *reinterpret_cast<uint2*>(xbp + ((size_t)wg * 32 + lane) * 2) = make_uint2(bf[0], bf[1]);
+        else
+            *reinterpret_cast<uint4*>(xbp + ((size_t)wg * 32 + lane) * 4) = make_uint4(bf[0], bf[1], bf[2], bf[3]);
+        st_shared_if(grp == 0, &xmp[h0 * GW + wg], e0);
+        st_shared_if(grp == 0, &xmp[h1 * GW + wg], e1);
+        st_shared_if(grp == 0, &xlp[h0 * GW + wg], l0);
+        st_shared_if(grp == 0, &xlp[h1 * GW + wg], l1);
+        // ---- rows past the sequence end hold stale data: zero this warp's dims of them,
+        // so that 0 * V stays 0
+        if (nvalid < kBK) {
+            constexpr int CPR = DW / 8;  // 16-byte chunks of a row in this warp's dims
+            const int nchunks = (kBK - nvalid) * CPR;
             for (int i = lane; i < nchunks; i += 32) {
-                const int row = r0 + i / (C::ROWB / 16), c = i % (C::ROWB / 16);
-                *reinterpret_cast<uint4*>(sV + rowoff(row) + (c >> 3) * PR * 128 + (c & 7) * 16) =
+                const int row = nvalid + i / CPR, c = wg * CPR + i % CPR;
+                *reinterpret_cast<uint4*>(sV + rowoff(row) + (c >> 3) * PR * 128 + (((c & 7) ^ (row & 7)) << 4)) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
-            __syncwarp();
         }
-        // ---- O^T partial of this block
+        named_bar_sync(1, GW * 32);
+        // ---- the block's max exponent and weight sum per head
+        {
+            const float4 mq0 = *reinterpret_cast<const float4*>(xmp + (u0 ? q0 : 0) * GW);
+            const float4 mq1 = *reinterpret_cast<const float4*>(xmp + (u1 ? q1 : 0) * GW);
+            const float4 lq0 = *reinterpret_cast<const float4*>(xlp + (u0 ? q0 : 0) * GW);
+            const float4 lq1 = *reinterpret_cast<const float4*>(xlp + (u1 ? q1 : 0) * GW);
+            const float emx0 = fmaxf(fmaxf(mq0.x, mq0.y), fmaxf(mq0.z, mq0.w));
+            const float emx1 = fmaxf(fmaxf(mq1.x, mq1.y), fmaxf(mq1.z, mq1.w));
+            auto wsum = [](const float4& m, const float4& l, float mx) {
+                float s = 0.f;
+                s += m.x == -INFINITY ? 0.f : exp2f(m.x - mx) * l.x;
+                s += m.y == -INFINITY ? 0.f : exp2f(m.y - mx) * l.y;
+                s += m.z == -INFINITY ? 0.f : exp2f(m.z - mx) * l.z;
+                s += m.w == -INFINITY ? 0.f : exp2f(m.w - mx) * l.w;
+                return s;
+            };
+            mbN[0] = u0 ? emx0 : -INFINITY;
+            mbN[1] = u1 ? emx1 : -INFINITY;
+            lbN[0] = u0 && emx0 != -INFINITY ? wsum(mq0, lq0, emx0) : 0.f;
+            lbN[1] = u1 && emx1 != -INFINITY ? wsum(mq1, lq1, emx1) : 0.f;
+        }
+        const float4 mb4 = *reinterpret_cast<const float4*>(xmp + hb * GW);
+        const float ebh = fmaxf(fmaxf(mb4.x, mb4.y), fmaxf(mb4.z, mb4.w));
+        const float mbw[4] = {mb4.x, mb4.y, mb4.z, mb4.w};
+        // ---- O^T of this warp's dims over the block's 64 keys, chunk by chunk
+#pragma unroll
+        for (int m = 0; m < MT; ++m) tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
         __syncwarp();
 #pragma unroll
-        for (int m = 0; m < KS; ++m) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(sw(vbase, keyV, 2 * m + chV), a0, a1, a2, a3);
-            tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
-            mma_bf16(tN[m], a0, a1, a2, a3, bh0, bh1);
-            if constexpr (!SPLITN) mma_bf16(tN[m], a0, a1, a2, a3, bl0, bl1);
+        for (int c = 0; c < GW; ++c) {
+            uint32_t b[XBW];
+            if constexpr (XBW == 2) {
+                const uint2 t2 = *reinterpret_cast<const uint2*>(xbp + ((size_t)c * 32 + lane) * 2);
+                b[0] = t2.x; b[1] = t2.y;
+            } else {
+                const uint4 t4 = *reinterpret_cast<const uint4*>(xbp + ((size_t)c * 32 + lane) * 4);
+                b[0] = t4.x; b[1] = t4.y; b[2] = t4.z; b[3] = t4.w;
+            }
+            const uint32_t sc2 = hb < G ? pow2_bf16x2(mbw[c], ebh) : 0u;
+#pragma unroll
+            for (int k = 0; k < XBW; ++k) b[k] = hmul2_bf16(b[k], sc2);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(sw(vbase, 16 * c + keyV, 2 * (wg * MT + m) + chV), a0, a1, a2, a3);
+                mma_bf16(tN[m], a0, a1, a2, a3, b[0], b[1]);
+                if constexpr (!SPLITN) mma_bf16(tN[m], a0, a1, a2, a3, b[2], b[3]);
+            }
         }
+        xpar ^= 1;
         __syncwarp();
         mbar_arrive_if(lane == 0, &empty[slot]);  // the slot's data are no longer read
         if (kART && mt.kind == kUBlock && !publish(mt, kUBlock, true)) return;
@@ -927,7 +1015,7 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
                     int quit = 0;
                     if (lane == 0) {
                         if (ld_volatile_shared(&ctrl->abort)) quit = 1;
-                        else if ((it & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+                        else if ((it & 63u) == 63u && global_ns() - t0 > ctrl->wait_ns) {
                             st_volatile_shared(&ctrl->abort, 1);
                             atomicOr(&p.hdr->status, ART_STATUS_TIMEOUT);
                             record_check(p.hdr, 252, item, kk, k);
@@ -1141,6 +1229,7 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     uint64_t* part_empty = part_full + kUnitRecs;
     uint64_t* ufull = part_empty + kUnitRecs;
     uint64_t* uempty = ufull + 1;
+    uint64_t* stall_bar = uempty + 1;  // never completed (the failure-path test hook)
     int* prank = reinterpret_cast<int*>(smem + L.ptab);
     URec* rinfo = reinterpret_cast<URec*>(smem + L.rinfo);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
@@ -1156,8 +1245,10 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
         }
         mbar_init(ufull, 1);
         mbar_init(uempty, 1);
+        mbar_init(stall_bar, 1);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
+        ctrl->wait_ns = p.wait_ns;
         fence_mbar_init();
     }
     if (tid < D) {
@@ -1176,6 +1267,7 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     }
     __syncthreads();
     const int warp = tid >> 5;
+    if (p.stall && warp < 4 && !wait_bounded(stall_bar, 0u, ctrl, p.hdr, 261 + 1)) return;
     if (warp == 4) {
         producer_u<C>(p, up, ring, meta, full, empty, ctrl, &tk, &tv);
     } else if (warp == 5) {
@@ -1193,24 +1285,18 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     }
 }
 
-// Per (item, query head, 32 head dims): merge the partials of the units before the
-// stopping unit and of the fix pieces (or of the stopping unit itself when it ends at
-// the stop), write O = sums / weight sums and blocks_used. Lane l holds head dim
-// 32 blockIdx.z + l; warp w takes partials w, w + 8, ..., 32 at a time: lane i loads
-// the max and weight sum of the i-th, then the warp adds their sums with all the loads
-// in flight together.
+// Per (item, query head): merge the partials of the units before the stopping unit and
+// of the fix pieces (or of the stopping unit itself when it ends at the stop), in list
+// order, and write O = sums / weight sums and blocks_used. Thread d holds head dim d.
 template <int D, int G>
-__global__ void __launch_bounds__(256) art_units_combine(const Params p, const UParams up0) {
+__global__ void __launch_bounds__(D) art_units_combine(const Params p, const UParams up0) {
     using E = Elem<true>;
     // launched while the unit kernel may still run: wait for it to finish
     asm volatile("griddepcontrol.wait;" ::: "memory");
     UParams up = up0;
     up.ck = p.hdr->ck;
-    __shared__ float s_m[8], s_l[8], s_o[8][32];
-    const int item = blockIdx.x, h = blockIdx.y;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d = 32 * blockIdx.z + lane;
-    const bool lead = threadIdx.x == 0 && h == 0 && blockIdx.z == 0;
+    const int item = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+    const bool lead = threadIdx.x == 0 && h == 0;
     const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
     const size_t obase = ((size_t)b * p.Hq + (size_t)g * G + h) * D;
     const ItemInfo inf = p.info[item];
@@ -1219,7 +1305,7 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
     const int t = n > 0 ? up.stop_min[item] : -1;
     if (bad || n == 0 || t < 0 || t >= n) {
         if (!bad && n > 0 && lead) record_check(p.hdr, 261, item, t, n);
-        if (w == 0) E::store(p.out, obase + d, 0.f);
+        E::store(p.out, obase + d, 0.f);
         if (lead && p.blocks_used) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
         return;
     }
@@ -1227,80 +1313,26 @@ __global__ void __launch_bounds__(256) art_units_combine(const Params p, const U
     const int kk = t / up.ck, sfirst = kk * up.ck;
     const bool use_fix = t != min(n, sfirst + up.ck) - 1;
     const int nunits = use_fix ? kk : kk + 1;        // whole units
-    const int npieces = use_fix ? t - sfirst + 1 : 0;  // fix pieces (one block each)
-    const int nq = (nunits + npieces) * 4;             // partials, 4 warps each
-    // fragment position of (h, d): lane 4 (d % 8) + h / 2, word 4 (d / 16) + 2 ((d / 8) % 2) + h % 2
-    const int off = (4 * (d & 7) + (h >> 1)) * (D / 4) + 4 * (d >> 4) + 2 * ((d >> 3) & 1) + (h & 1);
-    auto part_of = [&](int qi, const float*& po, const float*& pml) {
-        const int ui = qi >> 2;
-        size_t x;
-        if (ui < nunits) {
-            x = (size_t)item * up.maxk + ui;
-            po = up.part_o + x * 32 * D;
-            pml = up.part_ml + x * 64;
-        } else {
-            x = (size_t)item * up.ck + (ui - nunits);
-            po = up.fix_o + x * 32 * D;
-            pml = up.fix_ml + x * 64;
-        }
-        po += (size_t)(qi & 3) * 32 * (D / 4);
-        pml += (qi & 3) * 16;
+    const int nq = nunits + (use_fix ? t - sfirst + 1 : 0);  // ... then fix pieces (one block each)
+    const size_t ubase = (size_t)item * up.maxk, fbase = (size_t)item * up.ck - nunits;
+    auto ml_of = [&](int q) -> const float* {
+        return q < nunits ? up.part_ml + (ubase + q) * kUnitMlWords : up.fix_ml + (fbase + q) * kUnitMlWords;
     };
-    float M = -INFINITY, Lw = 0.f, O = 0.f;
-    for (int q0 = w; q0 < nq; q0 += 8 * 32) {
-        const int qi = q0 + 8 * lane;
-        float mi = -INFINITY, li = 0.f;
-        if (qi < nq) {
-            const float* po;
-            const float* pml;
-            part_of(qi, po, pml);
-            mi = pml[h];
-            li = pml[8 + h];
-        }
-        float mx = mi;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (mx == -INFINITY) continue;  // no partial here saw a valid key
-        const float Mn = fmaxf(M, mx);
-        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn);
-        const float fi = mi == -INFINITY ? 0.f : exp2f(mi - Mn);
-        Lw = fmaf(a, Lw, warp_sum(fi * li));
-        O *= a;
-        M = Mn;
-        const int cnt = min(32, (nq - q0 + 7) / 8);
-        float v[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-            v[x] = 0.f;
-            if (x < cnt) {
-                const float* po;
-                const float* pml;
-                part_of(q0 + 8 * x, po, pml);
-                v[x] = po[off];
-            }
-        }
-#pragma unroll
-        for (int x = 0; x < 32; ++x) O = fmaf(__shfl_sync(0xffffffffu, fi, x), v[x], O);
+    auto o_of = [&](int q) -> const float* {
+        return q < nunits ? up.part_o + (ubase + q) * G * D : up.fix_o + (fbase + q) * G * D;
+    };
+    float M = -INFINITY;
+    for (int q = 0; q < nq; ++q) M = fmaxf(M, __ldcg(ml_of(q) + h));
+    float num = 0.f, den = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < nq; ++q) {
+        const float* ml = ml_of(q);
+        const float mq = __ldcg(ml + h);
+        const float f = mq == -INFINITY ? 0.f : exp2f(mq - M);
+        num = fmaf(f, __ldcg(o_of(q) + h * D + d), num);
+        den = fmaf(f, __ldcg(ml + 8 + h), den);
     }
-    if (lane == 0) {
-        s_m[w] = M;
-        s_l[w] = Lw;
-    }
-    s_o[w][lane] = O;
-    __syncthreads();
-    if (w == 0) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) mx = fmaxf(mx, s_m[x]);
-        float num = 0.f, den = 0.f;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const float f = s_m[x] == -INFINITY ? 0.f : exp2f(s_m[x] - mx);
-            num = fmaf(f, s_o[x][lane], num);
-            den = fmaf(f, s_l[x], den);
-        }
-        E::store(p.out, obase + d, num / den);
-    }
+    E::store(p.out, obase + d, num / den);
 }
 
 // Largest ring depth (2..8 slots) that lets `want` CTAs share one SM.
@@ -1364,8 +1396,8 @@ cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* 
     // launch); it waits for the unit kernel's completion before reading anything
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(p.num_items, G, D / 32);
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3(p.num_items, G, 1);
+    cfg.blockDim = dim3(D);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

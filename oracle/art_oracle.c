@@ -10,8 +10,9 @@
  *   Scaled dot-product attention O = softmax(q K^T / sqrt(d)) V
  *   ("ART: Attention Run-time Termination", sec. 3.1, Eq. (1)), evaluated
  *   over the KV blocks of a visit list L in list order, together with the
- *   sequence of partial outputs O^(i) after the first i listed blocks
- *   (sec. 3.1: "O^(t) is the output after the first t blocks").
+ *   sequence of partial outputs O^(i), the attention output over only the
+ *   first i listed blocks (ART paper, sec. 3.1, the partial outputs of
+ *   block-wise attention).
  *
  *   The run-time termination rule (sec. 3.2 probe vector; explainer page
  *   gist.science "2.2 Stabilitaetsbasiertes Terminierungskriterium",

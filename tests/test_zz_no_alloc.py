@@ -68,6 +68,42 @@ def test_static_workspace_matches_caller_workspace(k, eps, p):
         assert rel <= REL_L2, f"call {call}: relative L2 {rel}"
 
 
+def test_static_status_after_bad_page_then_good_call():
+    """A call with one page id outside the pool (a bad host-side input that the
+    kernels check): that sequence's items get blocks_used = -1 and the array's
+    status word reports the bad page. The next call with good inputs on the same
+    array matches art_decode again."""
+    w = W.config(3, small=True)
+    dev = K.DeviceInputs(w)
+    f = _static_fn()
+    eps, p = 1e-2, 2
+    dev.art(eps, eps, p)
+    torch.cuda.synchronize()
+    ref_out = dev.out.float().cpu().numpy()
+    ref_bu = dev.blocks_used.cpu().numpy()
+    good_table = dev.block_table.clone()
+    dev.block_table[1, 0] = w.k_cache.shape[0] + 5  # sequence 1's first page: outside the pool
+    out = torch.zeros_like(dev.out)
+    bu = torch.full_like(dev.blocks_used, -7)
+    assert _call_static(f, dev, eps, p, out, bu) == K.ART_OK
+    torch.cuda.synchronize()
+    st = K.art_read_static_status()
+    assert st & 4, K.status_names(st)  # bad page id
+    got_bu = bu.cpu().numpy()
+    assert (got_bu[1] == -1).all()
+    assert np.array_equal(np.delete(got_bu, 1, axis=0), np.delete(ref_bu, 1, axis=0))
+    dev.block_table.copy_(good_table)
+    out = torch.full_like(dev.out, float("nan"))
+    bu = torch.full_like(dev.blocks_used, -7)
+    assert _call_static(f, dev, eps, p, out, bu) == K.ART_OK
+    torch.cuda.synchronize()
+    assert K.art_read_static_status() == 0
+    assert np.array_equal(bu.cpu().numpy(), ref_bu)
+    got = out.float().cpu().numpy()
+    assert np.abs(got - ref_out).max() <= MAX_ABS
+    assert np.linalg.norm(got - ref_out) / np.linalg.norm(ref_out) <= REL_L2
+
+
 def test_static_workspace_refuses_too_many_items():
     w = W.config(2, small=True)
     dev = K.DeviceInputs(w)

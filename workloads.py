@@ -374,3 +374,43 @@ def config(k: int, *, small: bool = False, eps: Optional[float] = None, patience
 
 
 CONFIG4_GRID = [(e, p) for e in (0.0, 1e-3, 1e-2) for p in (1, 2, 4)]
+
+
+# ----------------------------------------------------------------------------
+# partition by sequence (one GPU per shard; no exchange between shards)
+# ----------------------------------------------------------------------------
+def shard_range(batch: int, rank: int, world: int) -> tuple:
+    """Sequences [lo, hi) of shard `rank` of `world`: contiguous, sizes differing by
+    at most one, every sequence in exactly one shard."""
+    if not (1 <= world <= batch and 0 <= rank < world):
+        raise ValueError(f"{world} shards of a batch of {batch}")
+    return rank * batch // world, (rank + 1) * batch // world
+
+
+def shard_sequences(w: Workload, rank: int, world: int) -> Workload:
+    """The shard of `w` that owns sequences [lo, hi) (shard_range): their queries,
+    lengths, visit lists and block-table rows, and the pages those rows name,
+    gathered into a pool of their own (table entries renumbered in order of first
+    use). Items (b, g) of the shard are items (lo + b, g) of `w`."""
+    lo, hi = shard_range(w.batch, rank, world)
+    table = w.block_table[lo:hi]
+    pages_per_seq = -(-w.seq_lens[lo:hi].astype(np.int64) // w.page_size)
+    used = np.concatenate([table[i, : pages_per_seq[i]] for i in range(hi - lo)]) if hi > lo else \
+        np.zeros(0, np.int32)
+    phys, first = np.unique(used, return_index=True)
+    phys = phys[np.argsort(first, kind="stable")]  # order of first use
+    remap = {int(pg): i for i, pg in enumerate(phys)}
+    new_table = np.full_like(table, -1)
+    for i in range(hi - lo):
+        new_table[i, : pages_per_seq[i]] = [remap[int(x)] for x in table[i, : pages_per_seq[i]]]
+    k_cache = np.ascontiguousarray(w.k_cache[phys]) if phys.size else w.k_cache[:1].copy()
+    v_cache = np.ascontiguousarray(w.v_cache[phys]) if phys.size else w.v_cache[:1].copy()
+    notes = dict(w.notes, shard=dict(rank=rank, world=world, lo=lo, hi=hi))
+    return Workload(name=f"{w.name}-shard{rank}of{world}", dtype=w.dtype, batch=hi - lo,
+                    num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                    page_size=w.page_size, block_size=w.block_size,
+                    seq_lens=np.ascontiguousarray(w.seq_lens[lo:hi]), block_table=new_table,
+                    visit_order=None if w.visit_order is None else np.ascontiguousarray(w.visit_order[lo:hi]),
+                    q=np.ascontiguousarray(w.q[lo:hi]), k_cache=k_cache, v_cache=v_cache,
+                    probe_idx=w.probe_idx, eps_mag=w.eps_mag, eps_dir=w.eps_dir, patience=w.patience,
+                    notes=notes)
