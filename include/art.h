@@ -58,7 +58,10 @@
  *
  * Supported: dtype bf16 or fp32; head_dim 64 or 128; group size
  * G = num_q_heads / num_kv_heads in {1, 2, 4, 7, 8}; block_size 64;
- * page_size a power of two from 8 to 4096; num_probe 1..32.
+ * page_size a power of two from 8 to 4096; num_probe 1..32, or for bf16 up to
+ * head_dim (a probe over every head dim: the ablation of the gist.science
+ * explainer sec. 4 and the ART paper sec. 3.2, whose probe is a subset of the
+ * head dims; such calls always run one CTA per item).
  */
 #ifndef ART_H_
 #define ART_H_

@@ -372,7 +372,7 @@ static size_t unit_area_offset(int num_items) { return align_up(workspace_bytes_
 // path is offered); otherwise the unit path runs when there are fewer items
 // than half the SMs.
 static bool want_units(const art_shape& s, int patience, size_t workspace_bytes) {
-    if (!unit_eligible(s) || patience > kUnitBlocks) return false;
+    if (!unit_eligible(s) || patience > kUnitBlocks || s.num_probe > kMaxProbe) return false;
     const int items = s.batch * s.num_kv_heads;
     if (workspace_bytes < unit_area_offset(items) + unit_bytes(s)) return false;
     const char* env = std::getenv("ART_UNITS");
@@ -409,7 +409,8 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
     if (kART) {
         if (!probe_idx || !blocks_used) return ART_ERR_INVALID_ARG;
         if (s.num_probe < 1 || s.num_probe > s.head_dim) return ART_ERR_INVALID_ARG;
-        if (s.num_probe > kMaxProbe) return ART_ERR_UNSUPPORTED;
+        // more than kMaxProbe probe columns per head: bf16 only (one CTA per item)
+        if (s.num_probe > kMaxProbe && s.dtype != ART_DTYPE_BF16) return ART_ERR_UNSUPPORTED;
         if (patience < 1) return ART_ERR_INVALID_ARG;
         if (std::isnan(eps_mag) || std::isnan(eps_dir) || eps_mag < 0.f || eps_dir < 0.f) return ART_ERR_INVALID_ARG;
     }
@@ -439,6 +440,7 @@ static int run(const void* q, const void* k_cache, const void* v_cache, const in
         up.part_ml = reinterpret_cast<float*>(base + w.part_ml);
         up.fix_o = reinterpret_cast<float*>(base + w.fix_o);
         up.fix_ml = reinterpret_cast<float*>(base + w.fix_ml);
+        up.ustore = reinterpret_cast<float*>(base + w.ustore);
         up.ck = 0;  // chosen on the device by the plan kernel
         up.maxk = unit_maxk(s);
     }

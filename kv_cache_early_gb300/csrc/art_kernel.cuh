@@ -63,8 +63,11 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 enum Decision : int { kContinue = 0, kStop = 1, kDiscard = 2 };
 
 // kSplitDims: one group of four tensor-core warps with the head dims split (the unit
-// kernel's consumers); otherwise three or four groups split the dims, one or two the keys
-template <bool kBF16, int D, int G, int kNG = 1, bool kSplitDims = false>
+// kernel's consumers, and the variant for probes over more than kMaxProbe columns);
+// otherwise three or four groups split the dims, one or two the keys.
+// kMP: probe columns per query head at most (kMaxProbe, or D for a probe over every
+// head dim).
+template <bool kBF16, int D, int G, int kNG = 1, bool kSplitDims = false, int kMP = kMaxProbe>
 struct Cfg {
     using E = Elem<kBF16>;
     static constexpr bool TC = kBF16;            // bf16: tensor-core consumers on swizzled tiles
@@ -104,8 +107,9 @@ struct Cfg {
     // lane's pair of adjacent heads is one 8-byte store); rows padded by 8 words so
     // that the high- and low-part rows of the split tile fall in other banks
     static constexpr int GP = (G + 1) & ~1;
-    static constexpr int PST = kMaxProbe * GP + 8;
-    static constexpr int SPL = (kMaxProbe * GP + 31) / 32;  // probe slots per stat lane
+    static constexpr int MP = kMP;
+    static constexpr int PST = kMP * GP + 8;
+    static constexpr int SPL = (kMP * GP + 31) / 32;  // probe slots per stat lane
     static_assert(32 % GP == 0, "a stat lane's slots share one head");
     // G <= 4: the P.V products put the bf16 high parts of P in columns 0-3 of the
     // 8-wide tile and the low parts in columns 4-7, one mma per m-tile
@@ -1915,11 +1919,11 @@ struct MinBlocks {
     static constexpr int value = (C::TC && C::NG == 1) ? 2 : 1;
 };
 
-template <bool kBF16, int D, int G, int kNG, bool kART>
-__global__ void __launch_bounds__(Cfg<kBF16, D, G, kNG>::THREADS, (MinBlocks<Cfg<kBF16, D, G, kNG>>::value))
+template <class C, bool kART>
+__global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
     art_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
-    using C = Cfg<kBF16, D, G, kNG>;
     constexpr int NWC = C::NWC;
+    constexpr int D = C::DD;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the swizzled tiles need a 1024-byte aligned ring
     unsigned char* smem = smem_raw;
@@ -2065,11 +2069,11 @@ inline cudaError_t make_cache_map(CUtensorMap* m, const void* base, long long ro
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kBF16, int D, int G, int kNG, bool kART>
+template <class C, bool kART>
 cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, LaunchInfo* li, int sms, int smem_sm,
                            int smem_blk) {
-    using C = Cfg<kBF16, D, G, kNG>;
-    auto kern = art_decode_kernel<kBF16, D, G, kNG, kART>;
+    constexpr int D = C::DD;
+    auto kern = art_decode_kernel<C, kART>;
     cudaError_t e;
     // several CTAs per SM only pay when there are items for them
     const int per_sm = (p.num_items + sms - 1) / sms;
@@ -2124,14 +2128,25 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
     const char* env = std::getenv("ART_GROUPS");
     const int groups = env ? std::atoi(env) : (p.num_items >= 2 * sms ? 1 : p.num_items >= sms ? 2 : 3);
     if constexpr (kBF16) {
+        // a probe over more than kMaxProbe columns per head (up to every head dim): one
+        // group of four warps with the head dims split, so that each probe column has one
+        // writer and three records of probe rows fit in shared memory
+        if constexpr (kART)
+            if (p.m > kMaxProbe)
+                return launch_variant<Cfg<true, D, G, 1, true, D>, kART>(p, stream, force_stages, li, sms, smem_sm,
+                                                                           smem_blk);
+        // ART_SPLITDIMS=1: one group of four warps with the head dims split (else the keys)
+        const char* esd = std::getenv("ART_SPLITDIMS");
+        if (groups == 1 && esd && std::atoi(esd) != 0)
+            return launch_variant<Cfg<true, D, G, 1, true>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
         if (groups == 2)
-            return launch_variant<kBF16, D, G, 2, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+            return launch_variant<Cfg<kBF16, D, G, 2>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
         if (groups == 3)
-            return launch_variant<kBF16, D, G, 3, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+            return launch_variant<Cfg<kBF16, D, G, 3>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
         if (groups == 4)
-            return launch_variant<kBF16, D, G, 4, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+            return launch_variant<Cfg<kBF16, D, G, 4>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
     }
-    return launch_variant<kBF16, D, G, 1, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
+    return launch_variant<Cfg<kBF16, D, G, 1>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
 }
 
 }  // namespace art

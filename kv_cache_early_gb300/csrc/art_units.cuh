@@ -59,8 +59,9 @@ namespace art {
 
 constexpr int kUnitBlocks = 16;     // ck: ART blocks per unit at most
 constexpr int kUnitMinBlocks = 8;   // ... and at least (the workspace is sized for it)
-constexpr int kUnitRecs = 4;        // block records in flight from the consumers to the statistics warp
+constexpr int kUnitRecs = 5;        // block records in flight from the consumers to the statistics warp
 constexpr size_t kUnitMaxWsBytes = (size_t)4 << 30;  // the unit path's workspace area at most
+constexpr int kUnitMaxCtas = 512;   // unit-kernel CTAs at most (each has its own summary store)
 constexpr int kUnitMaxK = 4096;     // units per item at most
 constexpr int kUnitWords = 10;      // words per lane of a probe state: max, weight sum, 8 probe slots
 
@@ -82,7 +83,8 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
 
 // Byte offsets of the unit path's workspace area (after the one-CTA path's).
 struct UnitWs {
-    size_t p0, stop_min, resolved, fail, ulist, tflag, uflags, agg, incl, part_o, part_ml, fix_o, fix_ml, total;
+    size_t p0, stop_min, resolved, fail, ulist, tflag, uflags, agg, incl, part_o, part_ml, fix_o, fix_ml, ustore,
+        total;
 };
 
 // Partials are merged over the CTA's warps before they are written: per unit (and per
@@ -112,6 +114,7 @@ __host__ __device__ inline UnitWs make_unit_ws(int items, int maxk, int D, int G
     w.part_ml = take(U * kUnitMlWords * 4);
     w.fix_o = take((size_t)items * kUnitBlocks * G * D * 4);
     w.fix_ml = take((size_t)items * kUnitBlocks * kUnitMlWords * 4);
+    w.ustore = take((size_t)kUnitMaxCtas * 2 * kUnitBlocks * kUnitWords * 32 * 4);
     w.total = o;
     return w;
 }
@@ -130,6 +133,8 @@ struct UParams {
     float* part_ml;     // per (item, k): max of each head (words 0..7), weight sum (words 8..15)
     float* fix_o;       // per (item, fix piece): the piece's partial, same layout
     float* fix_ml;
+    float* ustore;      // per CTA: [2][kUnitBlocks][kUnitWords][32 lanes] block summaries of the units being
+                        // handed from the summary warp to the test warp (two in turn)
     int ck;             // ART blocks per unit (the kernels take it from the workspace header)
     int maxk;           // units per item at most
 };
@@ -149,23 +154,26 @@ struct UCfg {
     using C = Cfg<true, D, G, 1, true>;  // one group of four warps, head dims split
     static constexpr int THREADS = 7 * 32;  // 4 consumer warps, producer, block summaries, tests
     static constexpr int W = C::SPL + 2;
+    // a ring slot holds one block's K and V; the unit's queries go to their own tiles
+    static constexpr int SLOT = 2 * C::KVB;
+    static constexpr int QTB = 8 * C::ROWB;  // bytes of one query tile (8 rows, heads past G masked)
     static_assert(W <= kUnitWords, "probe state fits the workspace words");
 };
 
 struct ULayout {
-    size_t meta, bars, part, plb, pmb, qt, xb, ptab, rinfo, ust, uhdr, uagg, ctrl, total;
+    size_t meta, bars, part, plb, pmb, qt, xb, ptab, rinfo, uhdr, ctrl, total;
 };
 
 template <int D, int G>
 __host__ __device__ inline ULayout make_ulayout(int stages) {
     using C = typename UCfg<D, G>::C;
     ULayout L;
-    size_t o = (size_t)stages * C::SLOT;
+    size_t o = (size_t)stages * UCfg<D, G>::SLOT;
     L.meta = o;
     o += (size_t)stages * sizeof(UMeta);
     o = align_up(o, 16);
     L.bars = o;  // full[stages], empty[stages], part_full[NB], part_empty[NB]
-    o += (size_t)(2 * stages + 2 * kUnitRecs + 3) * sizeof(uint64_t);  // ... then ufull, uempty, stall
+    o += (size_t)(2 * stages + 2 * kUnitRecs + 7) * sizeof(uint64_t);  // ... ufull[2], uempty[2], stall, qfree[2]
     o = align_up(o, 16);
     static_assert(C::DS && C::RGW == 1, "one writer per probe column");
     L.part = o;  // [NB][PRW][PST] probe partial rows (one writer per column)
@@ -175,8 +183,8 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     L.pmb = o;  // [NB][G] block maxima (integer exponents)
     o += (size_t)kUnitRecs * G * sizeof(float);
     o = align_up(o, 1024);
-    L.qt = o;  // per consumer warp: the unit's queries, 8 rows (heads past G zero), 128B-swizzled
-    o += (size_t)C::GW * 8 * C::ROWB;
+    L.qt = o;  // two tiles of a unit's queries, 8 rows (heads past G masked), 128B-swizzled by the copy
+    o += (size_t)2 * UCfg<D, G>::QTB;
     o = align_up(o, 16);
     L.xb = o;  // [2 block parities][4 warps][32 lanes] P^T fragments, then [2][8][4] exponents,
                // then [2][8][4] weight sums
@@ -187,13 +195,8 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     L.rinfo = o;
     o += (size_t)kUnitRecs * sizeof(URec);
     o = align_up(o, 16);
-    L.ust = o;  // [ck][W][32 lanes] block summaries of the unit being tested
-    o += (size_t)kUnitBlocks * UCfg<D, G>::W * 32 * sizeof(float);
-    L.uhdr = o;  // the unit of the summaries
-    o += sizeof(URec);
-    o = align_up(o, 16);
-    L.uagg = o;  // [W][32 lanes] its probe aggregate
-    o += (size_t)UCfg<D, G>::W * 32 * sizeof(float);
+    L.uhdr = o;  // [2]: the units of the two summary buffers
+    o += 2 * sizeof(URec);
     o = align_up(o, 16);
     L.ctrl = o;  // only the abort and stop_item words of a Ctrl are used here
     static_assert(offsetof(Ctrl, abort) + sizeof(int) <= 128 && offsetof(Ctrl, stop_item) + sizeof(int) <= 128 &&
@@ -239,9 +242,10 @@ __device__ __forceinline__ bool poll_flag(const int* flag, int want, int& got, C
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
-template <class C>
+template <class C, class UC>
 __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ring, UMeta* meta, uint64_t* full,
-                           uint64_t* empty, Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv) {
+                           uint64_t* empty, uint64_t* qfree, unsigned char* qt, Ctrl* ctrl, const CUtensorMap* tk,
+                           const CUtensorMap* tv, const CUtensorMap* tq) {
     constexpr int G = C::GQ;
     constexpr int NH = C::ROWB / 128;
     const int lane = threadIdx.x & 31;
@@ -249,6 +253,7 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
     uint32_t round = 0;
     unsigned long long issued = 0;
     bool ok = true;
+    int uloc = 0;  // units of this CTA with blocks issued (selects the query tile)
     const int n_reg = p.hdr->n_regular, n_units = p.hdr->n_units;  // written by the plan kernel
 
     auto acquire = [&]() -> bool { return wait_bounded(&empty[slot], (round & 1u) ^ 1u, ctrl, p.hdr, 231); };
@@ -270,11 +275,174 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
         __syncwarp();
     };
 
+    // One listed position of a unit per lane (cnt <= 32): the logical block c, its valid
+    // tokens, the pages holding them (with pages larger than a block, the first row).
+    struct Pos {
+        int c, nvalid, npv, r0;
+        int pg[8];
+    };
+    // the position's pages; their loads are issued here, the values first used later
+    auto load_pages = [&](Pos& ps, int b, int seq_len, bool active) {
+        ps.nvalid = 0;
+        ps.npv = 0;
+        ps.r0 = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ps.pg[q] = 0;
+        const int t0 = ps.c * kBK;
+        if (!active || ps.c < 0 || t0 >= seq_len) return;
+        const int32_t* trow = p.block_table + (size_t)b * p.max_pages;
+        ps.nvalid = min(kBK, seq_len - t0);
+        if (p.Ps <= kBK) {
+            ps.npv = (ps.nvalid + p.Ps - 1) / p.Ps;
+            const int pfirst = t0 / p.Ps;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < ps.npv) ps.pg[q] = trow[pfirst + q];
+        } else {
+            ps.npv = 1;
+            ps.pg[0] = trow[t0 / p.Ps];
+            ps.r0 = t0 % p.Ps;
+        }
+    };
+    // a listed position outside the sequence or a page outside the pool
+    auto pos_bad = [&](const Pos& ps, int seq_len, bool active) -> bool {
+        if (!active) return false;
+        if (ps.c < 0 || ps.c * kBK >= seq_len) return true;
+        bool bad = false;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < ps.npv && (ps.pg[q] < 0 || ps.pg[q] >= p.num_pages)) bad = true;
+        return bad;
+    };
+
+    // ---- the next unit is claimed and resolved in steps (claim, list entry, item, visit
+    // entries, page ids), right after the current unit's last block is issued: the ring
+    // still holds that many blocks for the consumers meanwhile. (Claiming a unit while the
+    // current one is still being issued measured slower: a unit claimed early publishes its
+    // aggregate late, and the look-backs of later units of its item wait for it.)
+    int nst = 0;            // steps of the next unit done (5: resolved)
+    unsigned nclaim = 0;    // lane 0: the claim, until step 1
+    int nu = 0, nitem = -1, nk = 0, nb = 0, ng = 0, nn = 0, nfirst = 0, ncnt = 0, nseq = 0;
+    bool nend = false, nfix = false, nok = false;  // nok: a regular unit of a known item
+    int2 ne = make_int2(0, 0);
+    ItemInfo ninf;
+    ninf.n = 0;
+    ninf.flags = 0;
+    Pos np;
+    np.c = 0;
+    auto next_step = [&]() {
+        if (nst == 0) {
+            if (lane == 0) nclaim = atomicAdd(&p.hdr->uclaim, 1u);
+        } else if (nst == 1) {
+            nu = (int)__shfl_sync(0xffffffffu, nclaim, 0);
+            nend = nu >= n_units;
+            nfix = !nend && nu >= n_reg;
+            if (!nend && !nfix) ne = up.ulist[nu];
+        } else if (nst == 2) {
+            nok = false;
+            if (!nend && !nfix) {
+                nitem = ne.x;
+                nk = ne.y;
+                if (nitem >= 0 && nitem < p.num_items) {
+                    nok = true;
+                    ninf = p.info[nitem];
+                    nb = nitem / p.Hkv;
+                    ng = nitem - nb * p.Hkv;
+                    nseq = p.seq_lens[nb];
+                } else if (lane == 0) {
+                    record_check(p.hdr, 201, nu, nitem, 0);
+                }
+            }
+        } else if (nst == 3) {
+            if (nok) {
+                nn = (ninf.flags & kItemBad) ? 0 : ninf.n;
+                const int nch = (nn + up.ck - 1) / up.ck;
+                if (nk < 0 || nk >= nch) {
+                    if (lane == 0) record_check(p.hdr, 234, nitem, nk, nch);
+                    nok = false;
+                } else {
+                    nfirst = nk * up.ck;
+                    ncnt = min(up.ck, nn - nfirst);
+                    const int32_t* vrow = p.visit ? p.visit + (size_t)nitem * p.max_visit : nullptr;
+                    np.c = 0;
+                    if (lane < ncnt) np.c = vrow ? vrow[nfirst + lane] : nfirst + lane;
+                }
+            }
+        } else if (nst == 4) {
+            if (nok) load_pages(np, nb, nseq, lane < ncnt);
+        }
+        ++nst;
+    };
+
+    // issues the blocks of a unit (lanes hold its positions)
+    auto issue_unit = [&](bool fix, int item, int k, int first, int cnt, int n, int b, int g, const Pos& ps) -> bool {
+        for (int j = 0; j < cnt; ++j) {
+            if (!acquire()) return false;
+            const int cj = __shfl_sync(0xffffffffu, ps.c, j);
+            const int nvj = __shfl_sync(0xffffffffu, ps.nvalid, j);
+            const int npj = __shfl_sync(0xffffffffu, ps.npv, j);
+            const int r0j = __shfl_sync(0xffffffffu, ps.r0, j);
+            int pgj[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pgj[q] = __shfl_sync(0xffffffffu, ps.pg[q], j);
+            const bool with_q = j == 0;
+            // the unit's queries go to tile uloc % 2, once the consumers are done with the
+            // unit two before it (tiles alternate between units)
+            if (with_q && uloc >= 2 &&
+                !wait_bounded(&qfree[uloc & 1], (uint32_t)((uloc >> 1) - 1) & 1u, ctrl, p.hdr, 235))
+                return false;
+            const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
+            const uint32_t page_bytes = (uint32_t)(page_rows * C::ROWB);
+            const uint32_t bytes = 2u * npj * page_bytes + (with_q ? (uint32_t)UC::QTB : 0u);
+            unsigned char* dst = ring + (size_t)slot * UC::SLOT;
+            if (lane == 0) {
+                UMeta& mt = meta[slot];
+                mt.kind = fix ? kUFix : kUBlock; mt.item = item; mt.k = k; mt.j = j; mt.nj = cnt;
+                mt.pos = first + j; mt.n = n; mt.c = cj; mt.nvalid = nvj; mt.b = b; mt.g = g;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+            }
+            __syncwarp();
+            // each page's rows land as [column half][rows][128 B] (128B-swizzled), pages one
+            // after another; one 3-D copy per page, or one 2-D copy per column half
+            const int nop = p.tma3d ? npj : npj * NH;
+            const int nbox = 2 * nop;
+            const int nqc = with_q ? (p.tma3d ? 1 : NH) : 0;  // query copies: 8 rows from the group's first head
+            for (int t = lane; t < nbox + nqc; t += 32) {
+                if (t < nbox) {
+                    const int kv = t / nop;
+                    const int rem = t - kv * nop;
+                    const int q = p.tma3d ? rem : rem / NH, hf = p.tma3d ? 0 : rem - (rem / NH) * NH;
+                    int pk = 0;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        if (x == q) pk = pgj[x];
+                    const int y = (pk * p.Hkv + g) * p.Ps + r0j;
+                    unsigned char* d = dst + kv * C::KVB + (q * NH + hf) * page_rows * 128;
+                    if (p.tma3d)
+                        tma_load_3d(d, kv ? tv : tk, 0, y, 0, &full[slot]);
+                    else
+                        tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
+                } else {
+                    // rows past the group's G heads (the next group's, or zeros past the
+                    // tensor) only feed score columns the consumers mask
+                    unsigned char* qd = qt + (size_t)(uloc & 1) * UC::QTB;
+                    const int yq = b * p.Hq + g * G;
+                    if (p.tma3d)
+                        tma_load_3d(qd, tq, 0, yq, 0, &full[slot]);
+                    else
+                        tma_load_2d(qd + (t - nbox) * 1024, tq, (t - nbox) * 64, yq, &full[slot]);
+                }
+            }
+            __syncwarp();
+            advance();
+        }
+        ++uloc;
+        return true;
+    };
+
+    while (nst < 5) next_step();
     for (;;) {
-        int u = 0;
-        if (lane == 0) u = (int)atomicAdd(&p.hdr->uclaim, 1u);
-        u = __shfl_sync(0xffffffffu, u, 0);
-        if (u >= n_units) {
+        if (nend) {
             // nothing left to claim: the merge kernel may be launched
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             if (!acquire()) {
@@ -291,148 +459,94 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
             advance();
             break;
         }
-        const bool fix = u >= n_reg;
-        int item, k = 0;
-        if (!fix) {
-            const int2 e = up.ulist[u];
-            item = e.x;
-            k = e.y;
-        } else {
-            const int f = u - n_reg;  // fix piece f % ck of the item at claim position f / ck
-            item = p.order[f / up.ck];
-            k = f % up.ck;
-        }
-        if (item < 0 || item >= p.num_items) {
-            if (lane == 0) record_check(p.hdr, 201, u, item, 0);
+        if (nfix) {
+            // a fix piece (claimed after every regular unit): once every unit of its item has
+            // named its stop, block k of the stopping unit if it lies at or before the stop
+            const int f = nu - n_reg;  // fix piece f % ck of the item at claim position f / ck
+            nst = 0;
+            const int item = p.order[f / up.ck], k = f % up.ck;
+            bool skip = item < 0 || item >= p.num_items;
+            if (skip && lane == 0) record_check(p.hdr, 201, nu, item, 0);
+            int first = 0, n = 0, b = 0, g = 0, seq_len = 0;
+            if (!skip) {
+                const ItemInfo inf = p.info[item];
+                n = (inf.flags & kItemBad) ? 0 : inf.n;
+                const int nch = (n + up.ck - 1) / up.ck;
+                b = item / p.Hkv;
+                g = item - b * p.Hkv;
+                skip = nch == 0;
+                if (!skip) {
+                    int got = 0;
+                    if (!poll_flag(&up.resolved[item], nch, got, ctrl, p.hdr, 232)) {
+                        ok = false;
+                        break;
+                    }
+                    skip = ld_acquire_gpu(&up.fail[item]) != 0;
+                }
+                if (!skip) {
+                    const int t = ld_acquire_gpu(&up.stop_min[item]);
+                    if (t < 0 || t >= n) {
+                        if (lane == 0) record_check(p.hdr, 233, item, t, n);
+                        skip = true;
+                    } else {
+                        const int sfirst = t / up.ck * up.ck;
+                        // the stopping unit ends at the stop, or this piece's block lies past it
+                        skip = t == min(n, sfirst + up.ck) - 1 || sfirst + k > t;
+                        first = sfirst + k;
+                    }
+                }
+                if (!skip) seq_len = p.seq_lens[b];
+            }
+            if (!skip) {
+                Pos ps;
+                ps.c = 0;
+                if (lane == 0) {
+                    const int32_t* vrow = p.visit ? p.visit + (size_t)item * p.max_visit : nullptr;
+                    ps.c = vrow ? vrow[first] : first;
+                }
+                load_pages(ps, b, seq_len, lane == 0);
+                if (__any_sync(0xffffffffu, pos_bad(ps, seq_len, lane == 0))) {
+                    if (lane == 0) {
+                        atomicOr(&p.hdr->status, ART_STATUS_BAD_PAGE);
+                        atomicExch(&up.fail[item], 1);
+                    }
+                } else if (!issue_unit(true, item, k, first, 1, n, b, g, ps)) {
+                    ok = false;
+                    break;
+                }
+            }
+            while (nst < 5) next_step();
             continue;
         }
-        const ItemInfo inf = p.info[item];
-        const int n = (inf.flags & kItemBad) ? 0 : inf.n;
-        const int nch = (n + up.ck - 1) / up.ck;
-        const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
-        int first = 0, cnt = 0;
-        if (fix) {
-            if (nch == 0) continue;
-            int got = 0;
-            if (!poll_flag(&up.resolved[item], nch, got, ctrl, p.hdr, 232)) {
-                ok = false;
-                break;
-            }
-            if (ld_acquire_gpu(&up.fail[item])) continue;
-            const int t = ld_acquire_gpu(&up.stop_min[item]);
-            if (t < 0 || t >= n) {
-                if (lane == 0) record_check(p.hdr, 233, item, t, n);
-                continue;
-            }
-            const int sfirst = t / up.ck * up.ck;
-            if (t == min(n, sfirst + up.ck) - 1) continue;  // the stopping unit ends at the stop
-            if (sfirst + k > t) continue;                   // this piece's block lies past the stop
-            first = sfirst + k;
-            cnt = 1;
-        } else {
-            if (k < 0 || k >= nch) {
-                if (lane == 0) record_check(p.hdr, 234, item, k, nch);
-                continue;
-            }
-            first = k * up.ck;
-            cnt = min(up.ck, n - first);
-            if (ld_acquire_gpu(&up.stop_min[item]) < first) {
-                mark_skipped(item, k);
-                continue;
-            }
+        if (!nok) {
+            nst = 0;
+            while (nst < 5) next_step();
+            continue;
         }
-        // each lane resolves one listed position of the unit (cnt <= 32)
-        const int seq_len = p.seq_lens[b];
-        const int32_t* trow = p.block_table + (size_t)b * p.max_pages;
-        const int32_t* vrow = p.visit ? p.visit + (size_t)item * p.max_visit : nullptr;
-        int c = 0, nvalid = 0, npv = 0, bad = 0, r0 = 0;
-        int pg[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) pg[q] = 0;
-        if (lane < cnt) {
-            const int pos = first + lane;
-            c = vrow ? vrow[pos] : pos;
-            const int t0 = c * kBK;
-            if (c < 0 || t0 >= seq_len) {
-                bad = 1;
-            } else {
-                nvalid = min(kBK, seq_len - t0);
-                if (p.Ps <= kBK) {
-                    npv = (nvalid + p.Ps - 1) / p.Ps;
-                    const int pfirst = t0 / p.Ps;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        if (q < npv) pg[q] = trow[pfirst + q];
-                } else {
-                    npv = 1;
-                    pg[0] = trow[t0 / p.Ps];
-                    r0 = t0 % p.Ps;
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q < npv && (pg[q] < 0 || pg[q] >= p.num_pages)) bad = 1;
-            }
+        // the next unit becomes the current one
+        const int item = nitem, k = nk, b = nb, g = ng, n = nn, first = nfirst, cnt = ncnt, seq_len = nseq;
+        const Pos ps = np;
+        const int stop_seen = ld_acquire_gpu(&up.stop_min[item]);
+        nst = 0;
+        if (stop_seen < first) {  // the item stopped before this unit since it was claimed
+            mark_skipped(item, k);
+            while (nst < 5) next_step();
+            continue;
         }
-        if (__any_sync(0xffffffffu, bad)) {
+        if (__any_sync(0xffffffffu, pos_bad(ps, seq_len, lane < cnt))) {
             if (lane == 0) {
                 atomicOr(&p.hdr->status, ART_STATUS_BAD_PAGE);
                 atomicExch(&up.fail[item], 1);
             }
-            if (!fix) mark_skipped(item, k);
+            mark_skipped(item, k);
+            while (nst < 5) next_step();
             continue;
         }
-        for (int j = 0; j < cnt; ++j) {
-            if (!acquire()) {
-                ok = false;
-                break;
-            }
-            const int cj = __shfl_sync(0xffffffffu, c, j);
-            const int nvj = __shfl_sync(0xffffffffu, nvalid, j);
-            const int npj = __shfl_sync(0xffffffffu, npv, j);
-            const int r0j = __shfl_sync(0xffffffffu, r0, j);
-            int pgj[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) pgj[q] = __shfl_sync(0xffffffffu, pg[q], j);
-            const bool with_q = j == 0;
-            const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
-            const uint32_t page_bytes = (uint32_t)(page_rows * C::ROWB);
-            const uint32_t bytes = 2u * npj * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
-            unsigned char* dst = ring + (size_t)slot * C::SLOT;
-            if (lane == 0) {
-                UMeta& mt = meta[slot];
-                mt.kind = fix ? kUFix : kUBlock; mt.item = item; mt.k = k; mt.j = j; mt.nj = cnt;
-                mt.pos = first + j; mt.n = n; mt.c = cj; mt.nvalid = nvj; mt.b = b; mt.g = g;
-                mbar_arrive_expect_tx(&full[slot], bytes);
-            }
-            __syncwarp();
-            // each page's rows land as [column half][rows][128 B] (128B-swizzled), pages one
-            // after another; one 3-D copy per page, or one 2-D copy per column half
-            const int nop = p.tma3d ? npj : npj * NH;
-            const int nbox = 2 * nop;
-            for (int t = lane; t < nbox + (with_q ? 1 : 0); t += 32) {
-                if (t < nbox) {
-                    const int kv = t / nop;
-                    const int rem = t - kv * nop;
-                    const int q = p.tma3d ? rem : rem / NH, hf = p.tma3d ? 0 : rem - (rem / NH) * NH;
-                    int pk = 0;
-#pragma unroll
-                    for (int x = 0; x < 8; ++x)
-                        if (x == q) pk = pgj[x];
-                    const int y = (pk * p.Hkv + g) * p.Ps + r0j;
-                    unsigned char* d = dst + kv * C::KVB + (q * NH + hf) * page_rows * 128;
-                    if (p.tma3d)
-                        tma_load_3d(d, kv ? tv : tk, 0, y, 0, &full[slot]);
-                    else
-                        tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
-                } else {
-                    const char* src = static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
-                    bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
-                }
-            }
-            __syncwarp();
-            advance();
+        if (!issue_unit(false, item, k, first, cnt, n, b, g, ps)) {
+            ok = false;
+            break;
         }
-        if (!ok) break;
+        while (nst < 5) next_step();
     }
 
     if (!ok) {
@@ -468,10 +582,11 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
 // at once (no decision is waited for); at the unit's last block each warp writes
 // its own dims of the unit's partial.
 // ---------------------------------------------------------------------------
-template <class C, bool kART>
+template <class C, class UC, bool kART>
 __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ring, const UMeta* meta,
-                           uint64_t* full, uint64_t* empty, uint64_t* part_full, uint64_t* part_empty, URec* rinfo,
-                           const ULayout& L, unsigned char* smem, const int* prank, Ctrl* ctrl) {
+                           uint64_t* full, uint64_t* empty, uint64_t* part_full, uint64_t* part_empty,
+                           uint64_t* qfree, URec* rinfo, const ULayout& L, unsigned char* smem, const int* prank,
+                           Ctrl* ctrl) {
     constexpr int G = C::GQ, D = C::DD, KS = C::KS, GW = C::GW, NB = kUnitRecs;
     constexpr int DW = C::DW, MT = C::MT, XBW = C::XBW;
     constexpr bool SPLITN = C::SPLITN;
@@ -492,8 +607,9 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
     uint32_t* xb = reinterpret_cast<uint32_t*>(smem + L.xb);
     float* xm = reinterpret_cast<float*>(xb + 2 * GW * 32 * XBW);
     float* xl = xm + 2 * 8 * GW;
-    unsigned char* sQt = smem + L.qt + (size_t)wg * 8 * C::ROWB;  // this warp's copy of the unit's queries
-    const uint32_t qtbase = smem_addr(sQt);
+    const uint32_t qt0 = smem_addr(smem + L.qt);  // the two query tiles, used by alternate units
+    uint32_t qtbase = qt0;
+    int uloc = 0;  // units of this CTA seen (the producer's count)
     const float scale = 1.4426950408889634f / sqrtf((float)D);
     // this lane's O^T rows are d = wg DW + 16 mt + 8 r + grp; bit 2 mt + r marks a probe
     // dim, pofs[2 mt + r] the byte offset of its slot in a record's partial rows
@@ -656,21 +772,12 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
             if (kART) publish(endm, kUEnd, false);
             return;
         }
-        unsigned char* sK = ring + (size_t)slot * C::SLOT;
+        unsigned char* sK = ring + (size_t)slot * UC::SLOT;
         unsigned char* sV = sK + C::KVB;
         if (mt.j == 0) {
-            // the unit's queries into this warp's own swizzled 8-row area (rows past G zero)
+            // a new unit: its queries landed in tile uloc % 2 with this block
             reset();
-            const unsigned char* sQ = sK + 2 * C::KVB;
-            constexpr int QCH = 8 * (C::ROWB / 16);
-#pragma unroll
-            for (int i = lane; i < QCH; i += 32) {
-                const int row = i / (C::ROWB / 16), c = i % (C::ROWB / 16);
-                const uint4 val = row < G ? *reinterpret_cast<const uint4*>(sQ + (size_t)row * C::ROWB + c * 16)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sQt + (c >> 3) * 1024 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
-            }
-            __syncwarp();
+            qtbase = qt0 + (uint32_t)((uloc & 1) * UC::QTB);
         }
         const int nvalid = mt.nvalid;
         // ---- S^T for this warp's 16 keys (two independent accumulation chains)
@@ -691,6 +798,13 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
                 ldsm_x4(sw(kbase, keyK, 2 * ks + chK), a0, a1, a2, a3);
                 mma_bf16(h ? s4b : s4, a0, a1, a2, a3, h ? b10 : b00, h ? b11 : b01);
             }
+        }
+        const bool last = mt.j == mt.nj - 1;
+        if (last) {
+            // the unit's last read of its query tile: the producer may refill it
+            __syncwarp();
+            mbar_arrive_if(lane == 0, &qfree[uloc & 1]);
+            ++uloc;
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) s4[c] += s4b[c];
@@ -793,9 +907,15 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
         const float4 mb4 = *reinterpret_cast<const float4*>(xmp + hb * GW);
         const float ebh = fmaxf(fmaxf(mb4.x, mb4.y), fmaxf(mb4.z, mb4.w));
         const float mbw[4] = {mb4.x, mb4.y, mb4.z, mb4.w};
-        // ---- O^T of this warp's dims over the block's 64 keys, chunk by chunk
+        // ---- O^T of this warp's dims over the block's 64 keys, chunk by chunk, in two
+        // independent accumulator chains (even chunks or high parts into tN, odd chunks or
+        // low parts into tN2) that are added at the end
+        float tN2[MT][4];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
+        for (int m = 0; m < MT; ++m) {
+            tN[m][0] = tN[m][1] = tN[m][2] = tN[m][3] = 0.f;
+            tN2[m][0] = tN2[m][1] = tN2[m][2] = tN2[m][3] = 0.f;
+        }
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < GW; ++c) {
@@ -814,16 +934,24 @@ __device__ void consumer_u(const Params& p, const UParams& up, unsigned char* ri
             for (int m = 0; m < MT; ++m) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(sw(vbase, 16 * c + keyV, 2 * (wg * MT + m) + chV), a0, a1, a2, a3);
-                mma_bf16(tN[m], a0, a1, a2, a3, b[0], b[1]);
-                if constexpr (!SPLITN) mma_bf16(tN[m], a0, a1, a2, a3, b[2], b[3]);
+                if constexpr (SPLITN) {
+                    mma_bf16((c & 1) ? tN2[m] : tN[m], a0, a1, a2, a3, b[0], b[1]);
+                } else {
+                    mma_bf16(tN[m], a0, a1, a2, a3, b[0], b[1]);
+                    mma_bf16(tN2[m], a0, a1, a2, a3, b[2], b[3]);
+                }
             }
         }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tN[m][c] += tN2[m][c];
         xpar ^= 1;
         __syncwarp();
         mbar_arrive_if(lane == 0, &empty[slot]);  // the slot's data are no longer read
         if (kART && mt.kind == kUBlock && !publish(mt, kUBlock, true)) return;
         fold();
-        if (mt.j == mt.nj - 1) write_partial(mt);
+        if (last) write_partial(mt);
     }
 }
 
@@ -864,8 +992,9 @@ __device__ __forceinline__ void probe_slots(const Params& p, int lane, int (&hs)
 template <class C>
 __device__ void summ_u(const Params& p, const UParams& up, const float* part, const float* plb, const float* pmb,
                        uint64_t* part_full, uint64_t* part_empty, const URec* rinfo, float* ust, URec* uhdr,
-                       float* uagg, uint64_t* ufull, uint64_t* uempty, Ctrl* ctrl) {
+                       uint64_t* ufull, uint64_t* uempty, Ctrl* ctrl) {
     constexpr int G = C::GQ, SPL = C::SPL, RGW = C::RGW, W = SPL + 2;
+    constexpr int UBUF = kUnitBlocks * kUnitWords * 32;  // floats of one summary buffer
     constexpr int NPR = C::RGW * C::PRW;  // partial rows per record
     constexpr int UW = 32 * kUnitWords;   // floats of one probe state in the workspace
     const int lane = threadIdx.x & 31;
@@ -881,17 +1010,19 @@ __device__ void summ_u(const Params& p, const UParams& up, const float* part, co
         const URec ri = rinfo[rb];
         const bool valid = ri.kind == kUBlock && ri.j >= 0 && ri.j < ri.nj && ri.nj <= up.ck && ri.item >= 0 &&
                            ri.item < p.num_items && ri.k >= 0 && ri.k < up.maxk;
-        // a new unit (or the end) needs the summary buffer back from the test warp
-        if ((!valid || ri.j == 0) && urec >= 1 &&
-            !wait_bounded(uempty, (uint32_t)(urec - 1) & 1u, ctrl, p.hdr, 255))
+        // a new unit (or the end) needs its summary buffer (urec % 2) back from the test
+        // warp, which released it after the tests of the unit two before
+        const int ub = urec & 1;
+        if ((!valid || ri.j == 0) && urec >= 2 &&
+            !wait_bounded(&uempty[ub], (uint32_t)((urec >> 1) - 1) & 1u, ctrl, p.hdr, 255))
             return;
         if (!valid) {
             if (ri.kind == kUBlock && lane == 0) record_check(p.hdr, 254, ri.item, ri.k, ri.j);
             URec e = ri;
             e.kind = kUEnd;
-            if (lane == 0) *uhdr = e;
+            if (lane == 0) uhdr[ub] = e;
             __syncwarp();
-            mbar_arrive_if(lane == 0, ufull);
+            mbar_arrive_if(lane == 0, &ufull[ub]);
             return;
         }
         // block max and weight sum of this lane's head over the 4 warps (each used its own
@@ -925,7 +1056,7 @@ __device__ void summ_u(const Params& p, const UParams& up, const float* part, co
         }
         __syncwarp();
         mbar_arrive_if(lane == 0, &part_empty[rb]);
-        float* sm = ust + (size_t)ri.j * W * 32;
+        float* sm = ust + (size_t)ub * UBUF + (size_t)ri.j * W * 32;
         sm[lane] = mbk;
         sm[32 + lane] = lb;
 #pragma unroll
@@ -946,13 +1077,9 @@ __device__ void summ_u(const Params& p, const UParams& up, const float* part, co
             ga[32 + lane] = La;
 #pragma unroll
             for (int j = 0; j < SPL; ++j) ga[(2 + j) * 32 + lane] = Oa[j];
-            uagg[lane] = Ma;
-            uagg[32 + lane] = La;
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) uagg[(2 + j) * 32 + lane] = Oa[j];
-            if (lane == 0) *uhdr = ri;
+            if (lane == 0) uhdr[ub] = ri;
             __syncwarp();
-            mbar_arrive_if(lane == 0, ufull);
+            mbar_arrive_if(lane == 0, &ufull[ub]);  // the summaries and the aggregate are written
             ++urec;
             fence_acq_rel_gpu();
             __syncwarp();
@@ -966,13 +1093,15 @@ __device__ void summ_u(const Params& p, const UParams& up, const float* part, co
 // probe state before the unit, the stability tests of its blocks, and its stop
 // ---------------------------------------------------------------------------
 template <class C>
-__device__ void stat_u(const Params& p, const UParams& up, const float* ust, const URec* uhdr, const float* uagg,
-                       uint64_t* ufull, uint64_t* uempty, Ctrl* ctrl) {
-    bool released = false;  // the summary buffer has been handed back for the next unit
+__device__ void stat_u(const Params& p, const UParams& up, const float* ust, const URec* uhdr, uint64_t* ufull,
+                       uint64_t* uempty, Ctrl* ctrl) {
+    constexpr int UBUF = kUnitBlocks * kUnitWords * 32;  // floats of one summary buffer
+    bool released = false;  // the unit's summary buffer has been handed back to the summary warp
+    int ub = 0;             // ... which of the two
     auto release_buffer = [&]() {
         if (released) return;
         __syncwarp();
-        mbar_arrive_if((threadIdx.x & 31) == 0, uempty);
+        mbar_arrive_if((threadIdx.x & 31) == 0, &uempty[ub]);
         released = true;
     };
     constexpr int SPL = C::SPL;
@@ -985,12 +1114,15 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
 
     auto finish_unit = [&](int item, int k, int nj, const float* us) -> bool {
         const size_t iu = (size_t)item * up.maxk + k;
-        // the unit's own aggregate, handed over by the summary warp with the summaries
+        // the unit's own aggregate, written by the summary warp before it handed the unit over
         float Ma, La, Oa[SPL];
-        Ma = uagg[lane];
-        La = uagg[32 + lane];
+        {
+            const float* ga = up.agg + iu * UW;
+            Ma = ga[lane];
+            La = ga[32 + lane];
 #pragma unroll
-        for (int j = 0; j < SPL; ++j) Oa[j] = uagg[(2 + j) * 32 + lane];
+            for (int j = 0; j < SPL; ++j) Oa[j] = ga[(2 + j) * 32 + lane];
+        }
         // the probe state before this unit: aggregates of the earlier units, back to the
         // nearest one with an inclusive state
         float cM = -INFINITY, cL = 0.f, cO[SPL];
@@ -1096,32 +1228,47 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
             float v[4 * VS];
 #pragma unroll
             for (int j = 0; j < 4 * VS; ++j) v[j] = 0.f;
+            // the summaries (in global memory) are read four blocks at a time, with the
+            // loads of the four in flight together
+            constexpr int BQ = 4;
+            static_assert(kUnitBlocks % BQ == 0, "whole batches");
 #pragma unroll
-            for (int j = 0; j < kUnitBlocks; ++j) {
-                float s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                if (j < nj) {
-                    const float* s = us + (size_t)j * W * 32;
-                    const float mbk = s[lane], lb = s[32 + lane];
-                    const float Mn = fmaxf(M, mbk);
-                    const float a = exp2f(M - Mn);
-                    const float bw = exp2f(mbk - Mn);
-                    const float Ln = fmaf(a, Lsum, bw * lb);
-                    const float cf = __fdividef(bw, Ln);
-                    M = Mn;
-                    Lsum = Ln;
+            for (int j0 = 0; j0 < kUnitBlocks; j0 += BQ) {
+                float sv[BQ][W];
 #pragma unroll
-                    for (int jj = 0; jj < SPL; ++jj) {
-                        const float pb = s[(2 + jj) * 32 + lane];
-                        const float d = hs[jj] >= 0 ? cf * (pb - lb * X[jj]) : 0.f;
-                        s1 = fmaf(d, d, s1);
-                        s2 = fmaf(d, X[jj], s2);
-                        X[jj] += d;
-                        s3 = fmaf(X[jj], X[jj], s3);
-                    }
+                for (int q = 0; q < BQ; ++q) {
+                    const float* s = us + (size_t)(j0 + q) * W * 32;
+                    const bool live = j0 + q < nj;
+#pragma unroll
+                    for (int x = 0; x < W; ++x) sv[q][x] = live ? s[x * 32 + lane] : 0.f;
                 }
-                v[j] = s1;
-                v[VS + j] = s2;
-                v[2 * VS + j] = s3;
+#pragma unroll
+                for (int q = 0; q < BQ; ++q) {
+                    const int j = j0 + q;
+                    float s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                    if (j < nj) {
+                        const float mbk = sv[q][0], lb = sv[q][1];
+                        const float Mn = fmaxf(M, mbk);
+                        const float a = exp2f(M - Mn);
+                        const float bw = exp2f(mbk - Mn);
+                        const float Ln = fmaf(a, Lsum, bw * lb);
+                        const float cf = __fdividef(bw, Ln);
+                        M = Mn;
+                        Lsum = Ln;
+#pragma unroll
+                        for (int jj = 0; jj < SPL; ++jj) {
+                            const float pb = sv[q][2 + jj];
+                            const float d = hs[jj] >= 0 ? cf * (pb - lb * X[jj]) : 0.f;
+                            s1 = fmaf(d, d, s1);
+                            s2 = fmaf(d, X[jj], s2);
+                            X[jj] += d;
+                            s3 = fmaf(X[jj], X[jj], s3);
+                        }
+                    }
+                    v[j] = s1;
+                    v[VS + j] = s2;
+                    v[2 * VS + j] = s3;
+                }
             }
             release_buffer();  // the summaries are read: the summary warp may fill in the next unit's
             fence_acq_rel_gpu();
@@ -1198,11 +1345,12 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
     };
 
     for (int uu = 0;; ++uu) {
-        if (!wait_bounded(ufull, (uint32_t)uu & 1u, ctrl, p.hdr, 251)) return;
-        const URec ri = *uhdr;
+        ub = uu & 1;
+        if (!wait_bounded(&ufull[ub], (uint32_t)(uu >> 1) & 1u, ctrl, p.hdr, 251)) return;
+        const URec ri = uhdr[ub];
         if (ri.kind != kUBlock) return;
         released = false;
-        const bool done = finish_unit(ri.item, ri.k, ri.nj, ust);
+        const bool done = finish_unit(ri.item, ri.k, ri.nj, ust + (size_t)ub * UBUF);
         release_buffer();  // a unit whose item had stopped before it has not read its summaries
         if (!done) return;
     }
@@ -1214,10 +1362,11 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
 template <int D, int G, bool kART>
 __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     art_units_kernel(const Params p, const UParams up0, const __grid_constant__ CUtensorMap tk,
-                     const __grid_constant__ CUtensorMap tv) {
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
     UParams up = up0;
     up.ck = p.hdr->ck;  // chosen by the plan kernel
     using C = typename UCfg<D, G>::C;
+    using UC = UCfg<D, G>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const ULayout L = make_ulayout<D, G>(p.stages);
@@ -1227,9 +1376,11 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     uint64_t* empty = full + p.stages;
     uint64_t* part_full = empty + p.stages;
     uint64_t* part_empty = part_full + kUnitRecs;
-    uint64_t* ufull = part_empty + kUnitRecs;
-    uint64_t* uempty = ufull + 1;
-    uint64_t* stall_bar = uempty + 1;  // never completed (the failure-path test hook)
+    uint64_t* ufull = part_empty + kUnitRecs;  // [2]
+    uint64_t* uempty = ufull + 2;              // [2]
+    uint64_t* stall_bar = uempty + 2;  // never completed (the failure-path test hook)
+    uint64_t* qfree = stall_bar + 1;    // [2]: the consumers are done with a query tile
+    float* ust = up.ustore + (size_t)blockIdx.x * 2 * kUnitBlocks * kUnitWords * 32;  // this CTA's summary store
     int* prank = reinterpret_cast<int*>(smem + L.ptab);
     URec* rinfo = reinterpret_cast<URec*>(smem + L.rinfo);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
@@ -1243,9 +1394,13 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
             mbar_init(&part_full[b], C::GW);
             mbar_init(&part_empty[b], 1);
         }
-        mbar_init(ufull, 1);
-        mbar_init(uempty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ufull[b], 1);
+            mbar_init(&uempty[b], 1);
+        }
         mbar_init(stall_bar, 1);
+        mbar_init(&qfree[0], C::GW);
+        mbar_init(&qfree[1], C::GW);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
         ctrl->wait_ns = p.wait_ns;
@@ -1264,24 +1419,24 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     if (tid == 4 * 32) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
     }
     __syncthreads();
     const int warp = tid >> 5;
     if (p.stall && warp < 4 && !wait_bounded(stall_bar, 0u, ctrl, p.hdr, 261 + 1)) return;
     if (warp == 4) {
-        producer_u<C>(p, up, ring, meta, full, empty, ctrl, &tk, &tv);
+        producer_u<C, UC>(p, up, ring, meta, full, empty, qfree, smem + L.qt, ctrl, &tk, &tv, &tq);
     } else if (warp == 5) {
         if (kART)
             summ_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
                       reinterpret_cast<const float*>(smem + L.pmb), part_full, part_empty, rinfo,
-                      reinterpret_cast<float*>(smem + L.ust), reinterpret_cast<URec*>(smem + L.uhdr),
-                      reinterpret_cast<float*>(smem + L.uagg), ufull, uempty, ctrl);
+                      ust, reinterpret_cast<URec*>(smem + L.uhdr), ufull, uempty, ctrl);
     } else if (warp == 6) {
         if (kART)
-            stat_u<C>(p, up, reinterpret_cast<const float*>(smem + L.ust), reinterpret_cast<const URec*>(smem + L.uhdr),
-                      reinterpret_cast<const float*>(smem + L.uagg), ufull, uempty, ctrl);
+            stat_u<C>(p, up, ust, reinterpret_cast<const URec*>(smem + L.uhdr), ufull, uempty, ctrl);
     } else {
-        consumer_u<C, kART>(p, up, ring, meta, full, empty, part_full, part_empty, rinfo, L, smem, prank, ctrl);
+        consumer_u<C, UC, kART>(p, up, ring, meta, full, empty, part_full, part_empty, qfree, rinfo, L, smem, prank,
+                                ctrl);
     }
 }
 
@@ -1382,15 +1537,24 @@ cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* 
         if ((e = make_cache_map(&tk, p.k, rows, D, p.Ps)) != cudaSuccess) return e;
         if ((e = make_cache_map(&tv, p.v, rows, D, p.Ps)) != cudaSuccess) return e;
     }
+    // the queries [batch * Hq rows][D], read 8 rows (one group's heads and the next's) at a time
+    CUtensorMap tq;
+    std::memset(&tq, 0, sizeof tq);
+    const long long qrows = (long long)p.B * p.Hq;
+    if (p.tma3d) {
+        if ((e = make_cache_map3(&tq, p.q, qrows, D, 8)) != cudaSuccess) return e;
+    } else {
+        if ((e = make_cache_map(&tq, p.q, qrows, D, 8)) != cudaSuccess) return e;
+    }
     p.stages = stages;
-    const int grid = sms * occ;
+    const int grid = sms * occ < kUnitMaxCtas ? sms * occ : kUnitMaxCtas;
     if (li) {
         li->grid = grid;
         li->stages = stages;
         li->smem = smem;
         li->ctas_per_sm = occ;
     }
-    kern<<<grid, UCfg<D, G>::THREADS, smem, stream>>>(p, up, tk, tv);
+    kern<<<grid, UCfg<D, G>::THREADS, smem, stream>>>(p, up, tk, tv, tq);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // the merge kernel may start while the unit kernel drains (programmatic dependent
     // launch); it waits for the unit kernel's completion before reading anything

@@ -72,7 +72,8 @@ def call_art(lib, shape, q=FAKE, probe=FAKE, bu=FAKE, ws=FAKE, ws_bytes=1 << 20,
     (dict(shape=good_shape(page_size=4)), K.ART_ERR_UNSUPPORTED),
     (dict(shape=good_shape(dtype=5)), K.ART_ERR_INVALID_ARG),
     (dict(shape=good_shape(batch=0)), K.ART_ERR_INVALID_ARG),
-    (dict(shape=good_shape(num_probe=33)), K.ART_ERR_UNSUPPORTED),
+    (dict(shape=good_shape(num_probe=33, dtype=1)), K.ART_ERR_UNSUPPORTED),  # > 32 probe columns: bf16 only
+    (dict(shape=good_shape(num_probe=129)), K.ART_ERR_INVALID_ARG),  # more probe columns than head dims
     (dict(shape=good_shape(num_probe=0)), K.ART_ERR_INVALID_ARG),
     (dict(shape=good_shape(), patience=0), K.ART_ERR_INVALID_ARG),
     (dict(shape=good_shape(), em=float("nan")), K.ART_ERR_INVALID_ARG),
@@ -105,13 +106,13 @@ def test_workspace_size(lib):
     # one CTA per item: the 64-byte header, then per item {n, flags} and a claim-order slot
     s = good_shape(batch=3, num_kv_heads=4, num_q_heads=16, dtype=1)
     assert K.art_workspace_bytes(s) == 64 + 12 * 12
-    big = good_shape(batch=300, num_kv_heads=1, num_q_heads=1)  # bf16, more items than the unit path takes
-    assert K.art_workspace_bytes(big) == 64 + 12 * 300
-    # bf16 with few items: plus the unit path's area, which grows with the longest possible list
+    # bf16: plus the unit path's area, which grows with the items and the longest possible list
     small = good_shape(batch=3, num_kv_heads=4, num_q_heads=16)
     longer = good_shape(batch=3, num_kv_heads=4, num_q_heads=16, max_pages_per_seq=8 * 64)
     assert K.art_workspace_bytes(small) > 64 + 12 * 12
     assert K.art_workspace_bytes(longer) > K.art_workspace_bytes(small)
+    more = good_shape(batch=300, num_kv_heads=1, num_q_heads=1)
+    assert K.art_workspace_bytes(more) > 64 + 12 * 300
     assert lib.art_workspace_bytes(None) == 0
 
 
@@ -122,8 +123,9 @@ def test_status_strings(lib):
 
 def test_decode_path_choice(lib, monkeypatch):
     """Which kernel path a call takes (host logic only: with ART_UNITS set the
-    choice needs no device). The unit path is offered for bf16 with at most 256
-    items, patience at most 16 and a workspace that holds its area."""
+    choice needs no device). The unit path is offered for bf16 with patience at
+    most 16, at most 32 probe columns per head and a workspace that holds its
+    area."""
     monkeypatch.setenv("ART_UNITS", "1")
     small = good_shape(batch=3, num_kv_heads=4, num_q_heads=16)  # bf16, 12 items
     ws = K.art_workspace_bytes(small)
@@ -133,7 +135,9 @@ def test_decode_path_choice(lib, monkeypatch):
     assert K.art_decode_path(small, 2, 64 + 12 * 12) == 0  # the one-CTA path's workspace only
     assert K.art_decode_path(good_shape(batch=3, num_kv_heads=4, num_q_heads=16, dtype=1), 2, 1 << 30) == 0
     big = good_shape(batch=300, num_kv_heads=1, num_q_heads=1)  # 300 items
-    assert K.art_decode_path(big, 2, 1 << 30) == 0
+    assert K.art_decode_path(big, 2, K.art_workspace_bytes(big)) == 1
+    full = good_shape(batch=3, num_kv_heads=4, num_q_heads=16, num_probe=128)  # a probe over every head dim
+    assert K.art_decode_path(full, 2, K.art_workspace_bytes(full)) == 0
     assert K.art_decode_path(good_shape(head_dim=96), 2, 1 << 30) == 0  # fails the shape checks
     monkeypatch.setenv("ART_UNITS", "0")
     assert K.art_decode_path(small, 2, ws) == 0

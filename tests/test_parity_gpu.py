@@ -357,3 +357,34 @@ def test_probe_heads_option(small, k, monkeypatch):
             out = dev.out.float().cpu().numpy().reshape(w.num_items, w.group, w.head_dim)
             bu = dev.blocks_used.cpu().numpy().reshape(-1)
             check_art(w, out, bu, 1e-2, 1e-2, 2, what=f"probe heads {ph}, groups {groups}", probe_heads=ph)
+
+
+@pytest.mark.parametrize("k", [2, 4, 5])
+def test_probe_every_head_dim(small, k):
+    """A probe over every head dim (num_probe = head_dim, the full-d ablation): bf16
+    calls run one CTA per item with the head dims split between the four warps of a
+    group (one writer per probe column), against the oracle with the same probe."""
+    import dataclasses
+    w0 = small[k]
+    w = dataclasses.replace(w0, probe_idx=np.arange(w0.head_dim, dtype=np.int32))
+    for eps, p in ((1e-2, 2), (1e-3, 1), (0.0, 1)):
+        out, bu, st, _ = run_gpu(w, "art", eps, eps, p)
+        assert st == 0
+        res = check_art(w, out, bu, eps, eps, p, what=f"full-d probe, config {k}, eps {eps}, p {p}")
+        if eps == 0.0:
+            assert (bu == w.visit_lengths()).all()
+        print(res)
+
+
+@pytest.mark.parametrize("d,G", [(64, 8), (128, 1), (64, 2)])
+def test_probe_every_head_dim_shapes(d, G):
+    """The full-d probe on other head dims and group sizes (permuted 16-token pages,
+    ragged lengths)."""
+    w = W.build(f"fullprobe-d{d}-g{G}", seed=55 + d + G, dtype="bf16", batch=2, num_q_heads=2 * G, num_kv_heads=2,
+                head_dim=d, page_size=16, block_size=64, seq_lens=[1500, 777], paged="permuted", plant=True,
+                order="sink_recent", probe_stride=1)
+    assert w.num_probe == d
+    for eps, p in ((1e-2, 2), (3e-2, 1)):
+        out, bu, st, _ = run_gpu(w, "art", eps, eps, p)
+        assert st == 0
+        check_art(w, out, bu, eps, eps, p, what=f"full-d probe d {d} G {G}")
