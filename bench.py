@@ -374,6 +374,25 @@ def run_ours(args):
                  else "one CTA per item",
                  "kernel_gbs": (kv_bytes(w) + side_bytes(w)) / (ms_dk * 1e-3) / 1e9,
                  "speedup_art_over_dense": ms_d / ms}
+        # the dense twin on the other kernel path too (the path env override is read at
+        # each call): ART is also compared with the faster of the two full scans
+        saved = os.environ.get("ART_UNITS")
+        other = "0" if dense["path"] == "units" else "1"
+        os.environ["ART_UNITS"] = other
+        if K.art_decode_path(dev.shape, 1, dev.workspace.numel()) == int(other):
+            for _ in range(3):
+                dense_call()
+            t_o, t_ok = time_calls(dense_call, args.steps, kernel=True)
+            ms_o = float(t_o.mean())
+            best = min(ms_d, ms_o)
+            dense["other_path"] = {"path": "units" if other == "1" else "one CTA per item", "ms_per_step": ms_o,
+                                   "kernel_ms": float(t_ok.mean())}
+            dense["fastest_dense_ms_per_step"] = best
+            dense["speedup_art_over_fastest_dense"] = best / ms
+        if saved is None:
+            os.environ.pop("ART_UNITS", None)
+        else:
+            os.environ["ART_UNITS"] = saved
         # the detector's own cost: ART with eps = 0 never stops
         zero = lambda: dev.art(0.0, 0.0, p, stream=stream)
         for _ in range(3):

@@ -27,6 +27,6 @@ def test_default_path_follows_item_count(monkeypatch):
     for shape in cases:
         ws = K.art_workspace_bytes(shape)
         items = shape.batch * shape.num_kv_heads
-        expect = 1 if (2 * items < sms and items <= 256) else 0
+        expect = 1 if 2 * items < sms else 0
         assert K.art_decode_path(shape, 2, ws) == expect, (items, sms)
         assert K.art_decode_path(shape, 17, ws) == 0  # patience beyond the longest unit
