@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--shard", default="sequences", choices=["sequences", "replicas"],
                     help="N > 1: partition the workload's sequences over the ranks, or run a replica per rank")
+    ap.add_argument("--probe", default="stride4", choices=["stride4", "full"],
+                    help="the probe columns: every 4th head dim (the workloads' own), or every head dim")
     ap.add_argument("--diag", action="store_true",
                     help="print the convergence (O^(t) vs O^(T)) and score-vs-contribution diagnostics")
     ap.add_argument("--eps", type=float, default=None)
@@ -241,8 +243,18 @@ def config_dict(w, eps, p, ws, shard="sequences"):
                                         else f"{ws} independent replicas")
     return {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "page_size": w.page_size, "block_size": w.block_size, "eps": eps,
-            "patience": p, "l2": "flushed (256 MB write) before every timed call; inputs also exceed L2",
+            "patience": p, "probe_columns_per_head": int(w.num_probe),
+            "l2": "flushed (256 MB write) before every timed call; inputs also exceed L2",
             "parallelism": par}
+
+
+def load_workload(args):
+    """The workload of the command line; --probe full replaces the probe by every head dim."""
+    w = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)
+    if args.probe == "full":  # a probe over every head dim (the full-d ablation)
+        import dataclasses
+        w = dataclasses.replace(w, name=w.name + "-probe-full", probe_idx=np.arange(w.head_dim, dtype=np.int32))
+    return w
 
 
 # ---------------------------------------------------------------------------
@@ -252,7 +264,7 @@ def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    w = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)
+    w = load_workload(args)
     eps, p = w.eps_mag, w.patience
     import oracle as O
     # each step: the oracle over a bounded sample of items (at most ~10 s per step)
@@ -299,7 +311,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     B.build()
-    w_all = W.config(args.config, eps=args.eps, patience=args.patience, batch=args.batch)
+    w_all = load_workload(args)
     sharded = ws > 1 and args.shard == "sequences"
     # partition by sequence: this rank's slice of the one seeded workload; else a replica
     w = W.shard_sequences(w_all, rank, ws) if sharded else w_all

@@ -126,7 +126,7 @@ struct UParams {
     int* resolved;      // per item: units whose stop is named (or that were skipped)
     int* fail;          // per item: a page check failed in this path
     int* tflag;         // per (item, k): 1 aggregate, 2 and inclusive state, 3 skipped
-    int* uflags;        // per (item, k): {stable bits, blocks, state (1 set, 3 skipped), 0}
+    int* uflags;        // per (item, k): {stable bits, blocks, state (1 set, 3 skipped), resolved (1)}
     float* agg;         // per (item, k): [kUnitWords][32 lanes] probe state of the unit's blocks
     float* incl;        // per (item, k): the same through the unit (from the list's start)
     float* part_o;      // per (item, k): [G][D] output sums, merged over the warps
@@ -270,9 +270,54 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
         if (lane == 0) {
             st_release_gpu(&up.tflag[iu], 3);
             st_release_gpu(&up.uflags[4 * iu + 2], 3);
+            st_release_gpu(&up.uflags[4 * iu + 3], 1);
             red_release_add(&up.resolved[item], 1);
         }
         __syncwarp();
+    };
+    // Waits (bounded) until the item's stop is final and returns it: once every unit up to
+    // the one holding the smallest position named so far has been resolved, no unit can
+    // name a smaller one (later units start past it). Units after the stop need not have
+    // finished. Returns false on abort or timeout.
+    auto final_stop = [&](int item, int n, int& t_out) -> bool {
+        const unsigned long long t0 = global_ns();
+        for (unsigned it = 0;; ++it) {
+            int t = 0;
+            if (lane == 0) t = ld_acquire_gpu(&up.stop_min[item]);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t >= 0 && t < n) {
+                const int kk = t / up.ck;
+                bool all = true;
+                for (int base = 0; base <= kk && all; base += 32) {
+                    const int k = base + lane;
+                    const int r = k <= kk ? ld_acquire_gpu(&up.uflags[4 * ((size_t)item * up.maxk + k) + 3]) : 1;
+                    all = __all_sync(0xffffffffu, r >= 1);
+                }
+                if (all) {
+                    // a unit resolved after the first read may have named a smaller stop
+                    int t2 = 0;
+                    if (lane == 0) t2 = ld_acquire_gpu(&up.stop_min[item]);
+                    t2 = __shfl_sync(0xffffffffu, t2, 0);
+                    if (t2 == t) {
+                        t_out = t;
+                        return true;
+                    }
+                    continue;
+                }
+            }
+            int quit = 0;
+            if (lane == 0) {
+                if (ld_volatile_shared(&ctrl->abort)) quit = 1;
+                else if ((it & 63u) == 63u && global_ns() - t0 > ctrl->wait_ns) {
+                    st_volatile_shared(&ctrl->abort, 1);
+                    atomicOr(&p.hdr->status, ART_STATUS_TIMEOUT);
+                    record_check(p.hdr, 232, item, t, n);
+                    quit = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, quit, 0)) return false;
+            __nanosleep(64);
+        }
     };
 
     // One listed position of a unit per lane (cnt <= 32): the logical block c, its valid
@@ -475,16 +520,15 @@ __device__ void producer_u(const Params& p, const UParams& up, unsigned char* ri
                 b = item / p.Hkv;
                 g = item - b * p.Hkv;
                 skip = nch == 0;
+                int t = -1;
                 if (!skip) {
-                    int got = 0;
-                    if (!poll_flag(&up.resolved[item], nch, got, ctrl, p.hdr, 232)) {
+                    if (!final_stop(item, n, t)) {
                         ok = false;
                         break;
                     }
                     skip = ld_acquire_gpu(&up.fail[item]) != 0;
                 }
                 if (!skip) {
-                    const int t = ld_acquire_gpu(&up.stop_min[item]);
                     if (t < 0 || t >= n) {
                         if (lane == 0) record_check(p.hdr, 233, item, t, n);
                         skip = true;
@@ -1340,7 +1384,10 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
             }
         }
         __syncwarp();
-        if (lane == 0) red_release_add(&up.resolved[item], 1);  // after this lane's atomicMin and flags
+        if (lane == 0) {
+            st_release_gpu(up.uflags + 4 * iu + 3, 1);  // resolved: after this lane's atomicMin and flags
+            red_release_add(&up.resolved[item], 1);
+        }
         return true;
     };
 
@@ -1441,8 +1488,14 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
 }
 
 // Per (item, query head): merge the partials of the units before the stopping unit and
-// of the fix pieces (or of the stopping unit itself when it ends at the stop), in list
-// order, and write O = sums / weight sums and blocks_used. Thread d holds head dim d.
+// of the fix pieces (or of the stopping unit itself when it ends at the stop), and write
+// O = sums / weight sums and blocks_used. Thread d holds head dim d. The partials' maxima
+// and weight sums are first loaded into shared memory together (one load each, spread
+// over the threads), reduced to the common max and the weight sum, and turned into
+// factors; then each thread adds its dim's weighted sums, eight partials' loads in
+// flight at a time. The sums run in a fixed order (reproducible results).
+constexpr int kCombineMax = kUnitMaxK + kUnitBlocks;  // partials of one item at most
+
 template <int D, int G>
 __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UParams up0) {
     using E = Elem<true>;
@@ -1450,7 +1503,10 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     asm volatile("griddepcontrol.wait;" ::: "memory");
     UParams up = up0;
     up.ck = p.hdr->ck;
+    __shared__ float s_f[kCombineMax];  // the partials' maxima, then their factors
+    __shared__ float s_red[2][D / 32];
     const int item = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+    const int lane = d & 31, wq = d >> 5;
     const bool lead = threadIdx.x == 0 && h == 0;
     const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
     const size_t obase = ((size_t)b * p.Hq + (size_t)g * G + h) * D;
@@ -1467,8 +1523,12 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     if (lead && p.blocks_used) p.blocks_used[item] = t + 1;
     const int kk = t / up.ck, sfirst = kk * up.ck;
     const bool use_fix = t != min(n, sfirst + up.ck) - 1;
-    const int nunits = use_fix ? kk : kk + 1;        // whole units
+    const int nunits = use_fix ? kk : kk + 1;                // whole units
     const int nq = nunits + (use_fix ? t - sfirst + 1 : 0);  // ... then fix pieces (one block each)
+    if (nq > kCombineMax) {  // beyond the workspace's sizing: cannot happen for a checked plan
+        if (lead) record_check(p.hdr, 263, item, nq, kCombineMax);
+        return;
+    }
     const size_t ubase = (size_t)item * up.maxk, fbase = (size_t)item * up.ck - nunits;
     auto ml_of = [&](int q) -> const float* {
         return q < nunits ? up.part_ml + (ubase + q) * kUnitMlWords : up.fix_ml + (fbase + q) * kUnitMlWords;
@@ -1476,18 +1536,47 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     auto o_of = [&](int q) -> const float* {
         return q < nunits ? up.part_o + (ubase + q) * G * D : up.fix_o + (fbase + q) * G * D;
     };
-    float M = -INFINITY;
-    for (int q = 0; q < nq; ++q) M = fmaxf(M, __ldcg(ml_of(q) + h));
-    float num = 0.f, den = 0.f;
-#pragma unroll 4
-    for (int q = 0; q < nq; ++q) {
-        const float* ml = ml_of(q);
-        const float mq = __ldcg(ml + h);
-        const float f = mq == -INFINITY ? 0.f : exp2f(mq - M);
-        num = fmaf(f, __ldcg(o_of(q) + h * D + d), num);
-        den = fmaf(f, __ldcg(ml + 8 + h), den);
+    // the common max
+    float mx = -INFINITY;
+    for (int q = d; q < nq; q += D) {
+        const float m = __ldcg(ml_of(q) + h);
+        s_f[q] = m;
+        mx = fmaxf(mx, m);
     }
-    E::store(p.out, obase + d, num / den);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_red[0][wq] = mx;
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) M = fmaxf(M, s_red[0][w]);
+    // factors and the weight sum
+    float den = 0.f;
+    for (int q = d; q < nq; q += D) {
+        const float m = s_f[q];
+        const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+        s_f[q] = f;
+        den = fmaf(f, __ldcg(ml_of(q) + 8 + h), den);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane == 0) s_red[1][wq] = den;
+    __syncthreads();
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) L += s_red[1][w];
+    // this dim's weighted sums
+    float num = 0.f;
+    int q = 0;
+    for (; q + 8 <= nq; q += 8) {
+        float v[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) v[x] = __ldcg(o_of(q + x) + h * D + d);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) num = fmaf(s_f[q + x], v[x], num);
+    }
+    for (; q < nq; ++q) num = fmaf(s_f[q], __ldcg(o_of(q) + h * D + d), num);
+    E::store(p.out, obase + d, num / L);
 }
 
 // Largest ring depth (2..8 slots) that lets `want` CTAs share one SM.
