@@ -2137,10 +2137,6 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
             if (p.m > kMaxProbe)
                 return launch_variant<Cfg<true, D, G, 1, true, D>, kART>(p, stream, force_stages, li, sms, smem_sm,
                                                                            smem_blk);
-        // ART_SPLITDIMS=1: one group of four warps with the head dims split (else the keys)
-        const char* esd = std::getenv("ART_SPLITDIMS");
-        if (groups == 1 && esd && std::atoi(esd) != 0)
-            return launch_variant<Cfg<true, D, G, 1, true>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
         if (groups == 2)
             return launch_variant<Cfg<kBF16, D, G, 2>, kART>(p, stream, force_stages, li, sms, smem_sm, smem_blk);
         if (groups == 3)
