@@ -109,16 +109,19 @@ enum {
 };
 
 /* Bytes of device workspace art_decode / dense_decode need for `shape`.
- * Returns 0 if shape is NULL. For bf16 with batch * num_kv_heads <= 256 this
- * includes the area of the unit path (art_decode_path), which grows with
- * max_pages_per_seq * page_size (the longest possible list). */
+ * Returns 0 if shape is NULL. For bf16 this includes the area of the unit path
+ * (art_decode_path) when that area stays within 4 GiB; it grows with
+ * batch * num_kv_heads and with max_pages_per_seq * page_size (the longest
+ * possible list). A smaller workspace (at least the one-CTA path's part) keeps
+ * every call on the one-CTA path. */
 size_t art_workspace_bytes(const art_shape* shape);
 
 /*
  * Which kernel path art_decode takes for these arguments on the current device
  * (an addition of this library; the ART paper describes one CTA per sequence):
- *   0  one CTA per item (b, g): a persistent kernel whose CTAs claim whole
- *      items, longest lists first;
+ *   0  one CTA per item (b, g) at a time: a persistent kernel whose CTAs claim
+ *      whole items, longest lists first (bf16: one CTA per SM whose three
+ *      consumer groups take alternate blocks of the item);
  *   1  the unit path: each item's list is cut into units of 8 to 16 blocks
  *      (chosen per call so that the units fill whole waves of CTAs) that any
  *      CTA may take, so one item is spread over many SMs; the stop is
@@ -126,10 +129,10 @@ size_t art_workspace_bytes(const art_shape* shape);
  *      the stopping unit up to the stop are recomputed, and a second kernel
  *      merges the units' partial outputs. Blocks of units claimed before the
  *      stop was known are read and discarded.
- * The unit path is taken for bf16 when batch * num_kv_heads is at most 256 and
- * below the number of SMs / 2, patience <= 16 and workspace_bytes covers its
- * area; the environment variable ART_UNITS=0 or 1 forces the choice where the
- * path is offered. dense_decode takes the same path as art_decode with
+ * The unit path is taken for bf16 when batch * num_kv_heads is below the
+ * number of SMs / 2, patience <= 16, num_probe <= 32 and workspace_bytes covers
+ * its area; the environment variable ART_UNITS=0 or 1 forces the choice where
+ * the path is offered (any batch size). dense_decode takes the same path as art_decode with
  * patience 1 (there: all units, no statistics, no recompute). A shape that
  * fails the argument checks returns 0.
  */

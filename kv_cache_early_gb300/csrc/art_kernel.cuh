@@ -17,8 +17,11 @@
 //                    streaming softmax, O^(t) after t blocks). Three forms:
 //                    - fp32: 8 warps on CUDA cores (packed f32x2 FMA), each
 //                      owning 8 of the block's rows;
-//                    - bf16, one or two groups of 4 warps (keys split, below);
-//                    - bf16, three or four groups of 4 warps (dims split).
+//                    - bf16, groups of 4 warps with the head dims split: three
+//                      groups by default, or one for a probe over more than 32
+//                      columns per head;
+//                    - bf16, one or two groups of 4 warps with the keys split
+//                      (when forced with ART_GROUPS).
 //                    Several groups of one CTA take alternate blocks of the
 //                    same item and merge their accumulators at its end.
 //   statistics warp  (ART only) forms, in visit order, the probe x^(i) of O^(i)
@@ -1913,7 +1916,7 @@ __device__ void consumer_ds(const Params& p, unsigned char* ring, const SlotMeta
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-// tensor cores: one group per CTA runs two CTAs per SM; two or four groups one
+// tensor cores: one group per CTA runs two CTAs per SM; two to four groups one
 template <class C>
 struct MinBlocks {
     static constexpr int value = (C::TC && C::NG == 1) ? 2 : 1;

@@ -8,16 +8,18 @@
 //   plan        numbers the units round by round (unit k of every item, longest
 //               lists first, before unit k + 1 of any item), then ck fix pieces
 //               per item; CTAs claim units in that order from a counter.
-//   producer    TMA copies of a unit's blocks (with the queries at its first
-//               block) into the ring of shared-memory slots.
+//   producer    TMA copies of a unit's blocks into the ring of shared-memory
+//               slots, and of the unit's queries into one of two query tiles.
 //   consumers   softmax attention of each block for the G query heads (tensor
-//               cores, the 64 keys split over 4 warps, as in the one-CTA
-//               kernel), folded into the unit's partial output (per warp: a
-//               running max, weight sum and output sums), which goes to global
-//               memory at the unit's end; each block's probe partials go to the
-//               statistics warp.
-//   statistics  publishes the unit's probe aggregate (max, weight sum, probe
-//               sums per head) and takes the state of the probe before the unit
+//               cores, one group of 4 warps with the head dims split, as in the
+//               one-CTA kernel's default groups), folded into the unit's partial
+//               output (every warp: the same running max and weight sum, the
+//               output sums of its dims), which goes to global memory at the
+//               unit's end; each block's probe partials go to the summary warp.
+//   summary     turns each block's probe partials into a block summary (max,
+//               weight sum, probe sums per head), stored per CTA in global
+//               memory, and publishes the unit's probe aggregate.
+//   tests       takes the state of the probe before the unit
 //               from a look-back over the item's earlier units (their
 //               aggregates, back to the nearest one that has published its
 //               inclusive state). From that state it runs the stability test of
@@ -30,8 +32,9 @@
 //               Every position before the one-pass stop sees the same
 //               statistics as the one-pass rule, so the smallest position named
 //               is that stop.
-//   fix pieces  ck per item, claimed after every unit: once every unit of the
-//               item has named its stop (or been skipped), piece j recomputes
+//   fix pieces  ck per item, claimed after every unit: once every unit up to
+//               the one holding the item's stop has named its stop (or been
+//               skipped), piece j recomputes
 //               block j of the stopping unit if it lies at or before the stop
 //               (that unit's own partial also holds blocks after it), one block
 //               per CTA, so the recompute is spread over the GPU.
