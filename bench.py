@@ -382,7 +382,7 @@ def run_ours(args):
         t_d, t_dk = time_calls(dense_call, args.steps, kernel=True)
         ms_d, ms_dk = float(t_d.mean()), float(t_dk.mean())
         dense = {"queries_per_s": queries / (ms_d * 1e-3), "ms_per_step": ms_d, "kernel_ms": ms_dk,
-                 "path": "units" if K.art_decode_path(dev.shape, 1, dev.workspace.numel()) == 1
+                 "path": "units" if K.dense_decode_path(dev.shape, dev.workspace.numel()) == 1
                  else "one CTA per item",
                  "kernel_gbs": (kv_bytes(w) + side_bytes(w)) / (ms_dk * 1e-3) / 1e9,
                  "speedup_art_over_dense": ms_d / ms}
@@ -391,7 +391,7 @@ def run_ours(args):
         saved = os.environ.get("ART_UNITS")
         other = "0" if dense["path"] == "units" else "1"
         os.environ["ART_UNITS"] = other
-        if K.art_decode_path(dev.shape, 1, dev.workspace.numel()) == int(other):
+        if K.dense_decode_path(dev.shape, dev.workspace.numel()) == int(other):
             for _ in range(3):
                 dense_call()
             t_o, t_ok = time_calls(dense_call, args.steps, kernel=True)

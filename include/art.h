@@ -132,11 +132,17 @@ size_t art_workspace_bytes(const art_shape* shape);
  * The unit path is taken for bf16 when batch * num_kv_heads is below the
  * number of SMs / 2, patience <= 16, num_probe <= 32 and workspace_bytes covers
  * its area; the environment variable ART_UNITS=0 or 1 forces the choice where
- * the path is offered (any batch size). dense_decode takes the same path as art_decode with
- * patience 1 (there: all units, no statistics, no recompute). A shape that
- * fails the argument checks returns 0.
+ * the path is offered (any batch size). A shape that fails the argument checks
+ * returns 0.
  */
 int art_decode_path(const art_shape* shape, int32_t patience, size_t workspace_bytes);
+
+/* The kernel path dense_decode takes (0 or 1 as above). The full scan has no
+ * stop to find, so it takes the unit path (all units, no statistics, no
+ * recompute) whenever that path is offered: bf16 and a workspace that covers its
+ * area, at any batch size. ART_UNITS=0 or 1 forces the choice as above. An
+ * addition of this library. */
+int dense_decode_path(const art_shape* shape, size_t workspace_bytes);
 
 /*
  * ART decode attention (the method of the ART paper, sec. 3; the rule of the

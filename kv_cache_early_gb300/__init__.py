@@ -21,7 +21,8 @@ ART_DTYPE_BF16, ART_DTYPE_F32 = 0, 1
 ART_OK, ART_ERR_INVALID_ARG, ART_ERR_UNSUPPORTED, ART_ERR_WORKSPACE, ART_ERR_LAUNCH = 0, -1, -2, -3, -4
 STATUS_BITS = {1: "bad visit entry", 2: "duplicate visit entry", 4: "bad page id", 8: "bad seq_len",
                16: "bad probe index", 32: "wait timeout", 64: "internal check failed"}
-EXPORTS = ("art_workspace_bytes", "art_decode_path", "art_decode", "art_decode_ex", "dense_decode",
+EXPORTS = ("art_workspace_bytes", "art_decode_path", "dense_decode_path", "art_decode", "art_decode_ex",
+           "dense_decode",
            "art_decode_static", "art_read_static_status", "art_read_device_status",
            "art_status_string", "art_last_cuda_error", "art_set_timing_events",
            "art_select_workspace_bytes", "art_select_blocks")
@@ -60,6 +61,8 @@ def lib(path: str = LIB_PATH) -> ctypes.CDLL:
             L.art_workspace_bytes.restype = SZ
             L.art_decode_path.argtypes = [SP, I32, SZ]
             L.art_decode_path.restype = ctypes.c_int
+            L.dense_decode_path.argtypes = [SP, SZ]
+            L.dense_decode_path.restype = ctypes.c_int
             L.art_decode.argtypes = [P, P, P, P, P, P, F32, F32, I32, P, P, P, SP, P, SZ, P]
             L.art_decode.restype = ctypes.c_int
             L.dense_decode.argtypes = [P, P, P, P, P, P, P, SP, P, SZ, P]
@@ -124,6 +127,11 @@ def art_workspace_bytes(shape: ArtShape) -> int:
 def art_decode_path(shape: ArtShape, patience: int, workspace_bytes: int) -> int:
     """0: one CTA per item; 1: the unit path (see include/art.h)."""
     return int(lib().art_decode_path(ctypes.byref(shape), int(patience), int(workspace_bytes)))
+
+
+def dense_decode_path(shape: ArtShape, workspace_bytes: int) -> int:
+    """The kernel path dense_decode takes: 0 one CTA per item, 1 the unit path."""
+    return int(lib().dense_decode_path(ctypes.byref(shape), int(workspace_bytes)))
 
 
 def art_decode(q, k_cache, v_cache, block_table, seq_lens, visit_order, eps_mag, eps_dir, patience,

@@ -141,3 +141,19 @@ def test_decode_path_choice(lib, monkeypatch):
     assert K.art_decode_path(good_shape(head_dim=96), 2, 1 << 30) == 0  # fails the shape checks
     monkeypatch.setenv("ART_UNITS", "0")
     assert K.art_decode_path(small, 2, ws) == 0
+    assert K.dense_decode_path(small, ws) == 0
+
+
+def test_dense_path_choice(lib, monkeypatch):
+    """The dense twin takes the unit path whenever it is offered (bf16, a workspace
+    that holds its area), at any batch size; the choice needs no device."""
+    monkeypatch.delenv("ART_UNITS", raising=False)
+    for shape in (good_shape(batch=3, num_kv_heads=4, num_q_heads=16),
+                  good_shape(batch=300, num_kv_heads=1, num_q_heads=1),
+                  good_shape(batch=2, num_probe=128)):
+        ws = K.art_workspace_bytes(shape)
+        assert K.dense_decode_path(shape, ws) == 1
+        assert K.dense_decode_path(shape, 64 + 12 * shape.batch * shape.num_kv_heads) == 0  # one-CTA workspace only
+    fp32 = good_shape(dtype=1)
+    assert K.dense_decode_path(fp32, 1 << 30) == 0
+    assert K.dense_decode_path(good_shape(head_dim=96), 1 << 30) == 0
