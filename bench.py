@@ -411,7 +411,15 @@ def run_ours(args):
             zero()
         ms_z = float(time_calls(zero, args.steps).mean())
         dense["art_eps0_ms_per_step"] = ms_z
-        dense["detector_overhead_frac"] = ms_z / ms_d - 1.0
+        # against the full scan on ART's own kernel path, so that only the detector differs
+        art_on_units = K.art_decode_path(dev.shape, p, dev.workspace.numel()) == 1
+        same = ms_d if (dense["path"] == "units") == art_on_units else dense.get("other_path", {}).get("ms_per_step")
+        if same is not None:
+            dense["detector_overhead_frac"] = ms_z / same - 1.0
+            dense["detector_overhead_basis"] = "ART at eps 0 against the dense twin on the same kernel path ({})".format(
+                "units" if art_on_units else "one CTA per item")
+        if "fastest_dense_ms_per_step" in dense:
+            dense["art_eps0_over_fastest_dense"] = ms_z / dense["fastest_dense_ms_per_step"]
 
     # roofline of the decode kernel (bytes actually needed by the blocks processed)
     path = K.art_decode_path(dev.shape, p, dev.workspace.numel())

@@ -89,7 +89,12 @@ struct Cfg {
     static constexpr int RGW = DS ? 1 : GW;
     static constexpr int DW = D / GW;            // tensor-core path: head dims per consumer warp
     static constexpr int MT = DW / 16;           // ... and its O^T m-tiles
-    static constexpr int THREADS = (NWC + 2) * 32;
+    // tensor-core path with one CTA per SM (two or more groups): a copy warp issues the
+    // tensor copies of the entries the producer warp has resolved. A tensor copy holds
+    // the issuing warp for about as long as the copy engine takes to accept it; apart,
+    // the two warps' work overlaps. (Two CTAs per SM have two producers already.)
+    static constexpr bool COPYW = TC && NG >= 2;
+    static constexpr int THREADS = (NWC + 2 + (COPYW ? 1 : 0)) * 32;
     static constexpr int GQ = G;                 // query heads per KV head
     static constexpr int ELT = E::kBytes;
     static constexpr int DD = D;
@@ -136,6 +141,18 @@ struct SlotMeta {
     int item, pos, n, c, nvalid, kind, b, g, has0, pad0, pad1, pad2;
 };
 
+// What the copy warp loads into a ring entry (tensor-core path).
+enum JobKind : int { kJobData = 0, kJobNone = 1, kJobEnd = 2 };
+struct SlotJob {
+    int kind;    // kJobData: npg pages of K and of V (and the queries when with_q); otherwise no data
+    int npg;     // pages of the block, 1..8
+    int with_q;  // the entry also carries the item's queries
+    int b, g;    // sequence and KV head (the queries' address)
+    int y[8];    // first cache row of each page in the tensor map: (page * Hkv + g) * Ps + first row
+    int pad0, pad1, pad2;
+};
+static_assert(sizeof(SlotJob) == 64, "four 16-byte words");
+
 constexpr int kMaxNB = 16;  // record buffers at most (4 per consumer group)
 
 struct Ctrl {
@@ -148,7 +165,7 @@ struct Ctrl {
 static_assert(offsetof(Ctrl, wait_ns) % 8 == 0, "8-byte field");
 
 struct Layout {
-    size_t meta, bars, part, plb, pmb, wmax, scr, eacc, qt, xb, sh, ptab, ctrl, total;
+    size_t meta, job, bars, part, plb, pmb, wmax, scr, eacc, qt, xb, sh, ptab, ctrl, total;
 };
 
 template <class C>
@@ -159,8 +176,11 @@ __host__ __device__ inline Layout make_layout(int stages) {
     L.meta = o;
     o += (size_t)stages * sizeof(SlotMeta);
     o = align_up(o, 16);
+    L.job = o;  // copy warp: [stages] jobs
+    o += C::COPYW ? (size_t)stages * sizeof(SlotJob) : 0;
     L.bars = o;
-    o += (size_t)(2 * stages + 2 * C::NB + 2) * sizeof(uint64_t);  // ... cbar, then the stall barrier
+    // full, empty, record-full, decision [NB], cbar, the stall barrier, then the jobs' barriers
+    o += (size_t)(2 * stages + 2 * C::NB + 2 + (C::COPYW ? stages : 0)) * sizeof(uint64_t);
     o = align_up(o, 16);
     L.part = o;  // [NB][RGW][PRW][PST] probe partial rows
     o += (size_t)C::PART_F * sizeof(float);
@@ -263,9 +283,41 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctr
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
+// Tensor-core path: the copies of one block (npg pages of K, then of V) and, with
+// with_q, of the item's queries into the slot at dst, completing on bar (armed by the
+// caller). Each page's rows land as [column half][rows] (128-byte rows, 128B-swizzled),
+// pages one after another: one 3-D copy per page, or one 2-D copy per column half.
+// yof(k) is page k's first row in the tensor maps.
+template <class C, class YF>
+__device__ __forceinline__ void issue_block_tc(const Params& p, unsigned char* dst, int npg, bool with_q, int b, int g,
+                                               uint64_t* bar, const CUtensorMap* tk, const CUtensorMap* tv, YF yof) {
+    constexpr int NH = C::ROWB / 128;  // 128-byte column halves of a row
+    const int lane = threadIdx.x & 31;
+    const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
+    const int nop = p.tma3d ? npg : npg * NH;  // copies of K (and of V)
+    const int nbox = 2 * nop;
+    for (int t = lane; t < nbox + (with_q ? 1 : 0); t += 32) {
+        if (t < nbox) {
+            const int kv = t / nop;
+            const int rem = t - kv * nop;
+            const int k = p.tma3d ? rem : rem / NH, hf = p.tma3d ? 0 : rem - (rem / NH) * NH;
+            const int y = yof(k);
+            unsigned char* d = dst + kv * C::KVB + (k * NH + hf) * page_rows * 128;
+            if (p.tma3d)
+                tma_load_3d(d, kv ? tv : tk, 0, y, 0, bar);
+            else
+                tma_load_2d(d, kv ? tv : tk, hf * 64, y, bar);
+        } else {
+            const char* src = static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * C::GQ) * C::ROWB;
+            bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(C::GQ * C::ROWB), bar);
+        }
+    }
+}
+
 template <class C, bool kART>
-__device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* meta, uint64_t* full,
-                              uint64_t* empty, Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv) {
+__device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* meta, SlotJob* job, uint64_t* full,
+                              uint64_t* empty, uint64_t* jobb, Ctrl* ctrl, const CUtensorMap* tk,
+                              const CUtensorMap* tv) {
     constexpr int G = C::GQ;
     const int lane = threadIdx.x & 31;
     int slot = 0;
@@ -295,7 +347,12 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
             SlotMeta& mt = meta[slot];
             mt.item = item; mt.pos = pos; mt.n = n; mt.c = -1; mt.nvalid = 0; mt.kind = kind;
             mt.b = b; mt.g = g; mt.has0 = 0;
-            mbar_arrive(&full[slot]);
+            if constexpr (C::COPYW) {
+                job[slot].kind = kind == kSlotEnd ? kJobEnd : kJobNone;
+                mbar_arrive(&jobb[slot]);
+            } else {
+                mbar_arrive(&full[slot]);
+            }
         }
         __syncwarp();
         advance();
@@ -374,14 +431,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                 if (kART && ld_volatile_shared(&ctrl->stop_item) == item) { item_done = true; break; }
                 if (!acquire()) { ok = false; break; }
                 if (kART && ld_volatile_shared(&ctrl->stop_item) == item) { item_done = true; break; }
-                const int cj = __shfl_sync(0xffffffffu, c, j);
-                const int nvj = __shfl_sync(0xffffffffu, nvalid, j);
-                const int npj = __shfl_sync(0xffffffffu, npv, j);
                 const int badj = __shfl_sync(0xffffffffu, bad, j);
-                const int r0j = __shfl_sync(0xffffffffu, r0, j);
-                int pgj[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) pgj[k] = __shfl_sync(0xffffffffu, pg[k], j);
                 if (badj) {
                     if (lane == 0) atomicOr(&p.hdr->status, ART_STATUS_BAD_PAGE);
                     if (!(ok = emit(kSlotFail, item, b, g))) break;
@@ -391,62 +441,67 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
                 }
                 const int posj = base + j;
                 const bool with_q = posj < C::NG;  // each consumer group's first entry of the item
-                const uint32_t page_bytes = (uint32_t)((p.Ps <= kBK ? p.Ps : kBK) * C::ROWB);
-                const uint32_t bytes = 2u * npj * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
-                unsigned char* dst = ring + (size_t)slot * C::SLOT;
-                if (lane == 0) {
-                    SlotMeta& mt = meta[slot];
-                    mt.item = item; mt.pos = posj; mt.n = n; mt.c = cj; mt.nvalid = nvj; mt.kind = kSlotBlock;
-                    mt.b = b; mt.g = g; mt.has0 = inf.flags & kItemHas0;
-                    mbar_arrive_expect_tx(&full[slot], bytes);
-                }
-                __syncwarp();
-                if constexpr (C::TC) {
-                    // each page's rows land as [column half][rows] (128-byte rows, 128B-swizzled),
-                    // pages one after another; one 3-D copy per page, or one 2-D copy per half
-                    constexpr int NH = C::ROWB / 128;
-                    const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
-                    const int nop = p.tma3d ? npj : npj * NH;  // copies of K (and of V)
-                    const int nbox = 2 * nop;
-                    for (int t = lane; t < nbox + (with_q ? 1 : 0); t += 32) {
-                        if (t < nbox) {
-                            const int kv = t / nop;
-                            const int rem = t - kv * nop;
-                            const int k = p.tma3d ? rem : rem / NH, hf = p.tma3d ? 0 : rem - (rem / NH) * NH;
+                if constexpr (C::COPYW) {
+                    // the lane that resolved the position describes the entry; the copy warp
+                    // loads it and completes the slot's barrier
+                    if (lane == j) {
+                        SlotMeta& mt = meta[slot];
+                        mt.item = item; mt.pos = posj; mt.n = n; mt.c = c; mt.nvalid = nvalid; mt.kind = kSlotBlock;
+                        mt.b = b; mt.g = g; mt.has0 = inf.flags & kItemHas0;
+                        SlotJob& jb = job[slot];
+                        jb.kind = kJobData; jb.npg = npv; jb.with_q = with_q ? 1 : 0; jb.b = b; jb.g = g;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (k < npv) jb.y[k] = (pg[k] * p.Hkv + g) * p.Ps + r0;
+                        mbar_arrive(&jobb[slot]);
+                    }
+                } else {
+                    const int cj = __shfl_sync(0xffffffffu, c, j);
+                    const int nvj = __shfl_sync(0xffffffffu, nvalid, j);
+                    const int npj = __shfl_sync(0xffffffffu, npv, j);
+                    const int r0j = __shfl_sync(0xffffffffu, r0, j);
+                    int pgj[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) pgj[k] = __shfl_sync(0xffffffffu, pg[k], j);
+                    const uint32_t page_bytes = (uint32_t)((p.Ps <= kBK ? p.Ps : kBK) * C::ROWB);
+                    const uint32_t bytes = 2u * npj * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
+                    unsigned char* dst = ring + (size_t)slot * C::SLOT;
+                    if (lane == 0) {
+                        SlotMeta& mt = meta[slot];
+                        mt.item = item; mt.pos = posj; mt.n = n; mt.c = cj; mt.nvalid = nvj; mt.kind = kSlotBlock;
+                        mt.b = b; mt.g = g; mt.has0 = inf.flags & kItemHas0;
+                        mbar_arrive_expect_tx(&full[slot], bytes);
+                    }
+                    __syncwarp();
+                    if constexpr (C::TC) {
+                        issue_block_tc<C>(p, dst, npj, with_q, b, g, &full[slot], tk, tv, [&](int k) {
                             int pk = 0;
 #pragma unroll
                             for (int u = 0; u < 8; ++u)
                                 if (u == k) pk = pgj[u];
-                            const int y = (pk * p.Hkv + g) * p.Ps + r0j;
-                            unsigned char* d = dst + kv * C::KVB + (k * NH + hf) * page_rows * 128;
-                            if (p.tma3d)
-                                tma_load_3d(d, kv ? tv : tk, 0, y, 0, &full[slot]);
-                            else
-                                tma_load_2d(d, kv ? tv : tk, hf * 64, y, &full[slot]);
-                        } else {
-                            const char* src =
-                                static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
-                            bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
+                            return (pk * p.Hkv + g) * p.Ps + r0j;
+                        });
+                    } else {
+                        // one bulk copy per page of K and of V, and one of the queries
+                        const int ncopy = 2 * npj + (with_q ? 1 : 0);
+                        if (lane < ncopy) {
+                            if (lane < 2 * npj) {
+                                const int k = lane < npj ? lane : lane - npj;
+                                int pk = 0;
+#pragma unroll
+                                for (int t = 0; t < 8; ++t)
+                                    if (t == k) pk = pgj[t];
+                                const size_t row0 = ((size_t)pk * p.Hkv + g) * p.Ps + r0j;
+                                const char* src = (lane < npj ? kbase : vbase) + row0 * C::ROWB;
+                                unsigned char* d = dst + (lane < npj ? 0 : C::KVB) + (size_t)k * page_bytes;
+                                bulk_g2s(d, src, page_bytes, &full[slot]);
+                            } else {
+                                const char* src =
+                                    static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
+                                bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
+                            }
                         }
                     }
-                } else {
-                const int ncopy = 2 * npj + (with_q ? 1 : 0);
-                if (lane < ncopy) {
-                    if (lane < 2 * npj) {
-                        const int k = lane < npj ? lane : lane - npj;
-                        int pk = 0;
-#pragma unroll
-                        for (int t = 0; t < 8; ++t)
-                            if (t == k) pk = pgj[t];
-                        const size_t row0 = ((size_t)pk * p.Hkv + g) * p.Ps + r0j;
-                        const char* src = (lane < npj ? kbase : vbase) + row0 * C::ROWB;
-                        unsigned char* d = dst + (lane < npj ? 0 : C::KVB) + (size_t)k * page_bytes;
-                        bulk_g2s(d, src, page_bytes, &full[slot]);
-                    } else {
-                        const char* src = static_cast<const char*>(p.q) + ((size_t)b * p.Hq + (size_t)g * G) * C::ROWB;
-                        bulk_g2s(dst + 2 * C::KVB, src, (uint32_t)(G * C::ROWB), &full[slot]);
-                    }
-                }
                 }
                 __syncwarp();
                 advance();
@@ -461,8 +516,72 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
         if (!ok) break;
     }
 
+    if (!ok && !C::COPYW) {
+        // aborting: wait (bounded) for this CTA's own copies still in flight (the copy
+        // warp waits for those it issued)
+        const unsigned long long lim = issued < (unsigned long long)p.stages ? issued : p.stages;
+        int s = slot;
+        uint32_t r = round;
+        for (unsigned long long k = 0; k < lim; ++k) {
+            if (--s < 0) { s = p.stages - 1; --r; }
+            const unsigned long long t0 = global_ns();
+            while (!__all_sync(0xffffffffu, mbar_try_wait(&full[s], r & 1u)) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// copy warp (tensor-core path)
+// ---------------------------------------------------------------------------
+// Follows the ring in entry order: for each job the producer posted, it arms the
+// slot's full barrier with the entry's bytes and issues the tensor copies of its
+// pages (K, then V) and of the queries, or completes the barrier at once for an entry
+// without data. It leaves after the last consumer group's end entry.
+template <class C>
+__device__ void copy_warp(const Params& p, unsigned char* ring, const SlotJob* job, uint64_t* full, uint64_t* jobb,
+                          Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv) {
+    constexpr int G = C::GQ;
+    const int lane = threadIdx.x & 31;
+    const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
+    const uint32_t page_bytes = (uint32_t)(page_rows * C::ROWB);
+    int slot = 0, ends = 0;
+    uint32_t round = 0;
+    unsigned long long issued = 0;
+    bool ok = true;
+    for (;;) {
+        if (!wait_bounded<C::HINT>(&jobb[slot], round & 1u, ctrl, p.hdr, 171)) {
+            ok = false;
+            break;
+        }
+        const SlotJob* jb = &job[slot];
+        const int kind = jb->kind;
+        if (kind == kJobData) {
+            const int npg = jb->npg, with_q = jb->with_q;
+            if (npg < 1 || npg > 8) {
+                // not a job the producer writes: complete the slot without data
+                if (lane == 0) record_check(p.hdr, 6, slot, npg, 0);
+                mbar_arrive_if(lane == 0, &full[slot]);
+            } else {
+                const uint32_t bytes = 2u * npg * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
+                if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
+                __syncwarp();
+                issue_block_tc<C>(p, ring + (size_t)slot * C::SLOT, npg, with_q != 0, jb->b, jb->g, &full[slot], tk, tv,
+                                  [&](int k) { return jb->y[k]; });
+            }
+        } else {
+            mbar_arrive_if(lane == 0, &full[slot]);
+        }
+        __syncwarp();
+        ++issued;
+        if (++slot == p.stages) {
+            slot = 0;
+            ++round;
+        }
+        if (kind == kJobEnd && ++ends == C::NG) break;
+    }
     if (!ok) {
-        // aborting: wait (bounded) for this CTA's own copies still in flight
+        // aborting: wait (bounded) for the copies this warp issued that may still be in flight
         const unsigned long long lim = issued < (unsigned long long)p.stages ? issued : p.stages;
         int s = slot;
         uint32_t r = round;
@@ -1940,6 +2059,8 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
     uint64_t* dec_bar = part_full + C::NB;
     uint64_t* cbar = dec_bar + C::NB;
     uint64_t* stall_bar = cbar + 1;  // never completed (the failure-path test hook)
+    uint64_t* jobb = stall_bar + 1;  // copy warp: [stages] job posted
+    SlotJob* job = reinterpret_cast<SlotJob*>(smem + L.job);
     int* pmask = reinterpret_cast<int*>(smem + L.ptab);
     int* pbase = pmask + C::LPR;
     int* prank = pbase + C::LPR;
@@ -1958,6 +2079,8 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
         }
         mbar_init(cbar, NWC);
         mbar_init(stall_bar, 1);
+        if (C::COPYW)
+            for (int s = 0; s < p.stages; ++s) mbar_init(&jobb[s], 1);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
         ctrl->wait_ns = p.wait_ns;
@@ -1990,7 +2113,7 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
         }
         prank[tid] = found ? rank : -1;
     }
-    if (C::TC && tid == NWC * 32) {
+    if (C::TC && tid == (NWC + 2) * 32) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
     }
@@ -1999,7 +2122,9 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
     const int warp = tid >> 5;
     if (p.stall && warp < NWC && !wait_bounded(stall_bar, 0u, ctrl, p.hdr, 161)) return;
     if (warp == NWC) {
-        producer_warp<C, kART>(p, ring, meta, full, empty, ctrl, &tk, &tv);
+        producer_warp<C, kART>(p, ring, meta, job, full, empty, jobb, ctrl, &tk, &tv);
+    } else if (C::COPYW && warp == NWC + 2) {
+        copy_warp<C>(p, ring, job, full, jobb, ctrl, &tk, &tv);
     } else if (warp == NWC + 1) {
         if (kART)
             stat_warp<C>(p, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
