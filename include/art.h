@@ -121,7 +121,8 @@ size_t art_workspace_bytes(const art_shape* shape);
  * (an addition of this library; the ART paper describes one CTA per sequence):
  *   0  one CTA per item (b, g) at a time: a persistent kernel whose CTAs claim
  *      whole items, longest lists first (bf16: one CTA per SM whose three
- *      consumer groups take alternate blocks of the item);
+ *      consumer groups, four when there are no more items than SMs, take
+ *      alternate blocks of the item);
  *   1  the unit path: each item's list is cut into units of 8 to 16 blocks
  *      (chosen per call so that the units fill whole waves of CTAs) that any
  *      CTA may take, so one item is spread over many SMs; the stop is

@@ -137,7 +137,7 @@ struct Cfg {
     static_assert(G >= 1 && G <= 8, "group size");
 };
 
-struct SlotMeta {
+struct alignas(16) SlotMeta {  // read as three 16-byte words
     int item, pos, n, c, nvalid, kind, b, g, has0, pad0, pad1, pad2;
 };
 
@@ -643,7 +643,24 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
     for (int v = 0;; ++v) {
         const int vb = v % NB;
         if (!wait_bounded<C::HINT>(&part_full[vb], (uint32_t)(v / NB) & 1u, ctrl, p.hdr, 141)) return;
-        const SlotMeta* info = &ctrl->info[vb];
+        // every load of the record at once, ahead of the branches on its kind (for a
+        // record without a block the partial values are stale and go unused)
+        constexpr int RGW = C::RGW;
+        const SlotMeta rec = ctrl->info[vb];
+        float rmb[RGW], rlb[RGW], rpp[SPL][NP];
+#pragma unroll
+        for (int w = 0; w < RGW; ++w) {
+            rmb[w] = pmb[(vb * RGW + w) * G + hme];
+            rlb[w] = plb[(vb * RGW + w) * G + hme];
+        }
+        {
+            const float* pp = part + (size_t)vb * NP * C::PST;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j)
+#pragma unroll
+                for (int r = 0; r < NP; ++r) rpp[j][r] = pp[r * C::PST + lane + 32 * j];
+        }
+        const SlotMeta* info = &rec;
         const int kind = info->kind, item = info->item;
         if (kind == kSlotEnd) return;
         if (item == stopped_item || kind == kSlotPad) {
@@ -675,23 +692,22 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         // block max and sum of this lane's head over the consumer warps (each warp
         // used its own max), new running max and sum, and the factor that moves
         // the probe: delta = cf * (PV_probe - l_blk * x)
-        constexpr int RGW = C::RGW;
         float sw[RGW];
         float mbk = -INFINITY;
 #pragma unroll
         for (int w = 0; w < RGW; ++w) {
-            sw[w] = pmb[(vb * RGW + w) * G + hme];
+            sw[w] = rmb[w];
             mbk = fmaxf(mbk, sw[w]);
         }
         float lb = 0.f;
         if constexpr (RGW == 1) {
             sw[0] = 1.f;
-            lb = plb[vb * G + hme];
+            lb = rlb[0];
         } else {
 #pragma unroll
             for (int w = 0; w < RGW; ++w) {
                 sw[w] = sw[w] == -INFINITY ? 0.f : exp2f(sw[w] - mbk);  // a row set without valid keys adds nothing
-                lb = fmaf(sw[w], plb[(vb * RGW + w) * G + hme], lb);
+                lb = fmaf(sw[w], rlb[w], lb);
             }
         }
         const float Mn = fmaxf(M, mbk);
@@ -701,7 +717,6 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
         const float cf = __fdividef(bw, Ln);  // Ln >= 1/2: the block's largest weight is at least 1/2
         M = Mn;
         Lsum = Ln;
-        const float* pp = part + (size_t)vb * NP * C::PST;
         float s1 = 0.f, s2 = 0.f, s3 = 0.f;  // sum delta^2, sum delta . x_{i-1}, |x_i|^2
 #pragma unroll
         for (int j = 0; j < SPL; ++j) {
@@ -710,7 +725,7 @@ __device__ void stat_warp(const Params& p, const float* part, const float* plb, 
             for (int w = 0; w < RGW; ++w) {
                 float pw = 0.f;
 #pragma unroll
-                for (int r = 0; r < C::PRW; ++r) pw += pp[(w * C::PRW + r) * C::PST + lane + 32 * j];
+                for (int r = 0; r < C::PRW; ++r) pw += rpp[j][w * C::PRW + r];
                 pb = RGW == 1 ? pw : fmaf(sw[w], pw, pb);
             }
             // slots past the probe (or past G) hold no data: no change
@@ -2254,9 +2269,12 @@ cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchI
     // alternate blocks of an item. Measured against one group and two CTAs per SM (keys
     // split): 15 % faster on the ragged batch, 3 % on the paged one, and the statistics
     // cost 8 % instead of 15-20 %; the last item on an SM then also runs three blocks at a
-    // time. ART_GROUPS (1..4) overrides the choice.
+    // time. With no more items than SMs each CTA runs one item, whose blocks the consumer
+    // groups bound: four groups then (3 % faster on 128 items of 512 blocks; with more
+    // items, three groups and their deeper ring are 7 % faster). ART_GROUPS (1..4)
+    // overrides the choice.
     const char* env = std::getenv("ART_GROUPS");
-    const int groups = env ? std::atoi(env) : 3;
+    const int groups = env ? std::atoi(env) : (p.num_items <= sms ? 4 : 3);
     if constexpr (kBF16) {
         // a probe over more than kMaxProbe columns per head (up to every head dim): one
         // group of four warps with the head dims split, so that each probe column has one
