@@ -182,12 +182,23 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
-def kernel_source_hash():
+def kernel_source_hash(path=None):
+    """Hash of the CUDA sources a kernel path compiles from: "one CTA per item"
+    (the decode kernel, its instantiations and the plan kernel), "units" (the
+    unit and merge kernels, which also use the decode kernel's helpers), or
+    every source when path is None."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_early_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+        if not f.endswith((".cu", ".cuh")):
+            continue
+        if path is not None and f == "art_select.cu":
+            continue
+        if path == "one CTA per item" and f.startswith("art_units"):
+            continue
+        if path == "units" and f.startswith("art_inst_"):
+            continue
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -210,7 +221,7 @@ def load_traffic(config_name, alg_bytes, path):
         return None, None
     d = json.load(open(p))
     e = d.get(config_name)
-    if not e or e.get("kernel_hash") != kernel_source_hash() or e.get("path") != path:
+    if not e or e.get("kernel_hash") != kernel_source_hash(path) or e.get("path") != path:
         return None, None
     t = float(e["dram_bytes"]) * alg_bytes / float(e["algorithmic_bytes"])
     src = f"ncu capture of {e['captured_workload']}" + \
