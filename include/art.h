@@ -139,9 +139,10 @@ size_t art_workspace_bytes(const art_shape* shape);
 int art_decode_path(const art_shape* shape, int32_t patience, size_t workspace_bytes);
 
 /* The kernel path dense_decode takes (0 or 1 as above). The full scan has no
- * stop to find, so it takes the unit path (all units, no statistics, no
- * recompute) whenever that path is offered: bf16 and a workspace that covers its
- * area, at any batch size. ART_UNITS=0 or 1 forces the choice as above. An
+ * stop to find: it takes the unit path (all units, no statistics, no recompute)
+ * where that path is offered (bf16 and a workspace that covers its area) and
+ * batch * num_kv_heads is below the number of SMs; with more items one CTA per
+ * SM streams as fast or faster. ART_UNITS=0 or 1 forces the choice as above. An
  * addition of this library. */
 int dense_decode_path(const art_shape* shape, size_t workspace_bytes);
 

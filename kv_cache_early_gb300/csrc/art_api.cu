@@ -370,20 +370,23 @@ static size_t unit_area_offset(int num_items) { return align_up(workspace_bytes_
 
 // Unit path or one CTA per item: ART_UNITS=0/1 forces the choice (where the
 // path is offered). Otherwise ART takes the unit path when there are fewer items
-// than half the SMs, and the dense twin whenever the path is offered: its full
-// scan has no stop to find, and measured faster on the unit path at every batch
-// size (ragged batch 1.30 against 1.50 ms, paged 0.705 against 0.754 ms).
+// than half the SMs, and the dense twin when there are fewer items than SMs (its
+// full scan has no stop to find). Measured for the full scan: 128 items on 152
+// SMs 0.359 ms on units against 0.375 ms; with more items one CTA per SM is as
+// fast or faster (ragged batch 1.288 against 1.303 ms, paged 0.665 against 0.703).
 static bool want_units(const art_shape& s, int patience, size_t workspace_bytes, bool dense = false) {
     if (!unit_eligible(s) || (!dense && (patience > kUnitBlocks || s.num_probe > kMaxProbe))) return false;
     const int items = s.batch * s.num_kv_heads;
     if (workspace_bytes < unit_area_offset(items) + unit_bytes(s)) return false;
     const char* env = std::getenv("ART_UNITS");
     if (env) return std::atoi(env) != 0;
-    if (dense) return true;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    return 2 * items < sms;
+    // the full scan: units while some SM would get no item (with more items, one CTA
+    // per SM streams as fast or faster); ART: units below half the SMs (its
+    // statistics cost more per block on the unit path)
+    return dense ? items < sms : 2 * items < sms;
 }
 
 // events recorded around the decode-kernel launch of this thread's calls

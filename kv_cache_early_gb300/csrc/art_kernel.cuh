@@ -89,12 +89,15 @@ struct Cfg {
     static constexpr int RGW = DS ? 1 : GW;
     static constexpr int DW = D / GW;            // tensor-core path: head dims per consumer warp
     static constexpr int MT = DW / 16;           // ... and its O^T m-tiles
-    // tensor-core path with one CTA per SM (two or more groups): a copy warp issues the
-    // tensor copies of the entries the producer warp has resolved. A tensor copy holds
-    // the issuing warp for about as long as the copy engine takes to accept it; apart,
-    // the two warps' work overlaps. (Two CTAs per SM have two producers already.)
+    // tensor-core path with one CTA per SM (two or more groups): copy warps issue the
+    // tensor copies of the entries the producer warp has resolved, alternate entries
+    // each. A tensor copy holds the issuing warp for about as long as the copy engine
+    // takes to accept it; apart, the warps' work overlaps. (Two CTAs per SM have two
+    // producers already.)
     static constexpr bool COPYW = TC && NG >= 2;
-    static constexpr int THREADS = (NWC + 2 + (COPYW ? 1 : 0)) * 32;
+    // copy warps: two with three groups (whose ring depth is even), else one
+    static constexpr int NCW = COPYW ? (NG == 3 ? 2 : 1) : 0;
+    static constexpr int THREADS = (NWC + 2 + NCW) * 32;
     static constexpr int GQ = G;                 // query heads per KV head
     static constexpr int ELT = E::kBytes;
     static constexpr int DD = D;
@@ -176,8 +179,9 @@ __host__ __device__ inline Layout make_layout(int stages) {
     L.meta = o;
     o += (size_t)stages * sizeof(SlotMeta);
     o = align_up(o, 16);
-    L.job = o;  // copy warp: [stages] jobs
-    o += C::COPYW ? (size_t)stages * sizeof(SlotJob) : 0;
+    L.job = o;  // copy warps: [stages] jobs, then [stages] the last data entry each slot received
+    o += C::COPYW ? (size_t)stages * (sizeof(SlotJob) + sizeof(int)) : 0;
+    o = align_up(o, 16);
     L.bars = o;
     // full, empty, record-full, decision [NB], cbar, the stall barrier, then the jobs' barriers
     o += (size_t)(2 * stages + 2 * C::NB + 2 + (C::COPYW ? stages : 0)) * sizeof(uint64_t);
@@ -349,6 +353,7 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
             mt.b = b; mt.g = g; mt.has0 = 0;
             if constexpr (C::COPYW) {
                 job[slot].kind = kind == kSlotEnd ? kJobEnd : kJobNone;
+                job[slot].npg = pos;  // an end entry: its index among the NG end entries
                 mbar_arrive(&jobb[slot]);
             } else {
                 mbar_arrive(&full[slot]);
@@ -534,23 +539,32 @@ __device__ void producer_warp(const Params& p, unsigned char* ring, SlotMeta* me
 // ---------------------------------------------------------------------------
 // copy warp (tensor-core path)
 // ---------------------------------------------------------------------------
-// Follows the ring in entry order: for each job the producer posted, it arms the
-// slot's full barrier with the entry's bytes and issues the tensor copies of its
-// pages (K, then V) and of the queries, or completes the barrier at once for an entry
-// without data. It leaves after the last consumer group's end entry.
+// Copy warp cw of NCW takes the ring entries u = cw, cw + NCW, ... in order: for each
+// job the producer posted, it arms the slot's full barrier with the entry's bytes and
+// issues the tensor copies of its pages (K, then V) and of the queries, or completes
+// the barrier at once for an entry without data. The ring depth is a multiple of NCW,
+// so a slot's entries u, u + stages, ... all belong to one copy warp: the job barrier
+// phase a warp waits for is neither older than its previous entry in the slot (which
+// it has taken) nor newer (a slot is posted again only once consumed, which needs
+// this warp's copies). It leaves after its last entry among the consumer groups' NG
+// end entries (NG >= NCW, so every copy warp takes one of them). last[s] holds the
+// last data entry slot s received; on an abort each copy warp waits for the copies of
+// the slots whose last entry is its own (a later entry in a slot means the earlier
+// one was consumed).
 template <class C>
-__device__ void copy_warp(const Params& p, unsigned char* ring, const SlotJob* job, uint64_t* full, uint64_t* jobb,
-                          Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv) {
-    constexpr int G = C::GQ;
+__device__ void copy_warp(const Params& p, unsigned char* ring, const SlotJob* job, int* last, uint64_t* full,
+                          uint64_t* jobb, Ctrl* ctrl, const CUtensorMap* tk, const CUtensorMap* tv, int cw) {
+    constexpr int G = C::GQ, NCW = C::NCW;
+    static_assert(C::NG >= NCW, "every copy warp takes an end entry");
     const int lane = threadIdx.x & 31;
     const int page_rows = p.Ps <= kBK ? p.Ps : kBK;
     const uint32_t page_bytes = (uint32_t)(page_rows * C::ROWB);
-    int slot = 0, ends = 0;
-    uint32_t round = 0;
-    unsigned long long issued = 0;
+    int end_last = -1;  // the last end entry, once one end entry has been seen
     bool ok = true;
-    for (;;) {
-        if (!wait_bounded<C::HINT>(&jobb[slot], round & 1u, ctrl, p.hdr, 171)) {
+    for (int u = cw;; u += NCW) {
+        if (end_last >= 0 && u > end_last) break;
+        const int slot = u % p.stages;
+        if (!wait_bounded<C::HINT>(&jobb[slot], (uint32_t)(u / p.stages) & 1u, ctrl, p.hdr, 171)) {
             ok = false;
             break;
         }
@@ -564,31 +578,31 @@ __device__ void copy_warp(const Params& p, unsigned char* ring, const SlotJob* j
                 mbar_arrive_if(lane == 0, &full[slot]);
             } else {
                 const uint32_t bytes = 2u * npg * page_bytes + (with_q ? (uint32_t)(G * C::ROWB) : 0u);
-                if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
+                if (lane == 0) {
+                    last[slot] = u;
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                }
                 __syncwarp();
                 issue_block_tc<C>(p, ring + (size_t)slot * C::SLOT, npg, with_q != 0, jb->b, jb->g, &full[slot], tk, tv,
                                   [&](int k) { return jb->y[k]; });
             }
         } else {
+            if (kind == kJobEnd) {
+                const int k = jb->npg;  // its index among the end entries
+                end_last = u + (C::NG - 1 - (k >= 0 && k < C::NG ? k : C::NG - 1));
+            }
             mbar_arrive_if(lane == 0, &full[slot]);
         }
         __syncwarp();
-        ++issued;
-        if (++slot == p.stages) {
-            slot = 0;
-            ++round;
-        }
-        if (kind == kJobEnd && ++ends == C::NG) break;
     }
     if (!ok) {
         // aborting: wait (bounded) for the copies this warp issued that may still be in flight
-        const unsigned long long lim = issued < (unsigned long long)p.stages ? issued : p.stages;
-        int s = slot;
-        uint32_t r = round;
-        for (unsigned long long k = 0; k < lim; ++k) {
-            if (--s < 0) { s = p.stages - 1; --r; }
+        for (int s = 0; s < p.stages; ++s) {
+            const int v = ld_volatile_shared(&last[s]);
+            if (v < 0 || v % NCW != cw) continue;
             const unsigned long long t0 = global_ns();
-            while (!__all_sync(0xffffffffu, mbar_try_wait(&full[s], r & 1u)) && global_ns() - t0 < kWaitLimitNs) {
+            while (!__all_sync(0xffffffffu, mbar_try_wait(&full[s], (uint32_t)(v / p.stages) & 1u)) &&
+                   global_ns() - t0 < kWaitLimitNs) {
             }
         }
     }
@@ -2074,8 +2088,9 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
     uint64_t* dec_bar = part_full + C::NB;
     uint64_t* cbar = dec_bar + C::NB;
     uint64_t* stall_bar = cbar + 1;  // never completed (the failure-path test hook)
-    uint64_t* jobb = stall_bar + 1;  // copy warp: [stages] job posted
+    uint64_t* jobb = stall_bar + 1;  // copy warps: [stages] job posted
     SlotJob* job = reinterpret_cast<SlotJob*>(smem + L.job);
+    int* last_entry = reinterpret_cast<int*>(job + p.stages);
     int* pmask = reinterpret_cast<int*>(smem + L.ptab);
     int* pbase = pmask + C::LPR;
     int* prank = pbase + C::LPR;
@@ -2095,7 +2110,10 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
         mbar_init(cbar, NWC);
         mbar_init(stall_bar, 1);
         if (C::COPYW)
-            for (int s = 0; s < p.stages; ++s) mbar_init(&jobb[s], 1);
+            for (int s = 0; s < p.stages; ++s) {
+                mbar_init(&jobb[s], 1);
+                last_entry[s] = -1;
+            }
         ctrl->stop_item = -1;
         ctrl->abort = 0;
         ctrl->wait_ns = p.wait_ns;
@@ -2138,8 +2156,8 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
     if (p.stall && warp < NWC && !wait_bounded(stall_bar, 0u, ctrl, p.hdr, 161)) return;
     if (warp == NWC) {
         producer_warp<C, kART>(p, ring, meta, job, full, empty, jobb, ctrl, &tk, &tv);
-    } else if (C::COPYW && warp == NWC + 2) {
-        copy_warp<C>(p, ring, job, full, jobb, ctrl, &tk, &tv);
+    } else if (C::COPYW && warp >= NWC + 2) {
+        copy_warp<C>(p, ring, job, last_entry, full, jobb, ctrl, &tk, &tv, warp - (NWC + 2));
     } else if (warp == NWC + 1) {
         if (kART)
             stat_warp<C>(p, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
@@ -2223,7 +2241,8 @@ cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, Laun
     const int want = MinBlocks<C>::value < per_sm ? MinBlocks<C>::value : per_sm;
     int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(want, smem_sm, smem_blk);
     if (stages == 0) stages = pick_stages<C>(1, smem_sm, smem_blk);
-    if (stages == 0) return cudaErrorInvalidConfiguration;
+    if (C::NCW > 1) stages -= stages % C::NCW;  // every slot's entries go to one copy warp
+    if (stages < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = make_layout<C>(stages).total;
     if ((int)smem > smem_blk) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)

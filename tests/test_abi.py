@@ -145,9 +145,11 @@ def test_decode_path_choice(lib, monkeypatch):
 
 
 def test_dense_path_choice(lib, monkeypatch):
-    """The dense twin takes the unit path whenever it is offered (bf16, a workspace
-    that holds its area), at any batch size; the choice needs no device."""
-    monkeypatch.delenv("ART_UNITS", raising=False)
+    """The dense twin's unit path is offered for bf16 with a workspace that holds
+    its area, at any batch size and probe width (ART_UNITS=1 takes it wherever it
+    is offered; the default, which compares the item count with the SM count, is
+    checked on the device)."""
+    monkeypatch.setenv("ART_UNITS", "1")
     for shape in (good_shape(batch=3, num_kv_heads=4, num_q_heads=16),
                   good_shape(batch=300, num_kv_heads=1, num_q_heads=1),
                   good_shape(batch=2, num_probe=128)):

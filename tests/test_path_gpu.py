@@ -1,6 +1,6 @@
 """The default kernel path on the device: for ART, the unit path (one item over
 many CTAs) for bf16 calls with fewer items than half the SMs, one CTA per item
-otherwise; for the dense twin, the unit path whenever it is offered. Both paths
+otherwise; for the dense twin, the unit path with fewer items than SMs. Both paths
 give the oracle's result (the parity tests run every case on both with
 ART_UNITS)."""
 import pytest
@@ -31,4 +31,4 @@ def test_default_path_follows_item_count(monkeypatch):
         expect = 1 if 2 * items < sms else 0
         assert K.art_decode_path(shape, 2, ws) == expect, (items, sms)
         assert K.art_decode_path(shape, 17, ws) == 0  # patience beyond the longest unit
-        assert K.dense_decode_path(shape, ws) == 1  # the full scan: the unit path at any batch size
+        assert K.dense_decode_path(shape, ws) == (1 if items < sms else 0), (items, sms)
