@@ -176,7 +176,7 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     o += (size_t)stages * sizeof(UMeta);
     o = align_up(o, 16);
     L.bars = o;  // full[stages], empty[stages], part_full[NB], part_empty[NB]
-    o += (size_t)(2 * stages + 2 * kUnitRecs + 7) * sizeof(uint64_t);  // ... ufull[2], uempty[2], stall, qfree[2]
+    o += (size_t)(2 * stages + 2 * kUnitRecs + 9) * sizeof(uint64_t);  // ... ufull[2], uempty[2], stall, qfree[2], ustart[2]
     o = align_up(o, 16);
     static_assert(C::DS && C::RGW == 1, "one writer per probe column");
     L.part = o;  // [NB][PRW][PST] probe partial rows (one writer per column)
@@ -198,8 +198,8 @@ __host__ __device__ inline ULayout make_ulayout(int stages) {
     L.rinfo = o;
     o += (size_t)kUnitRecs * sizeof(URec);
     o = align_up(o, 16);
-    L.uhdr = o;  // [2]: the units of the two summary buffers
-    o += 2 * sizeof(URec);
+    L.uhdr = o;  // [2]: the units of the two summary buffers, then [2]: the units started in them
+    o += 4 * sizeof(URec);
     o = align_up(o, 16);
     L.ctrl = o;  // only the abort and stop_item words of a Ctrl are used here
     static_assert(offsetof(Ctrl, abort) + sizeof(int) <= 128 && offsetof(Ctrl, stop_item) + sizeof(int) <= 128 &&
@@ -1039,7 +1039,7 @@ __device__ __forceinline__ void probe_slots(const Params& p, int lane, int (&hs)
 template <class C>
 __device__ void summ_u(const Params& p, const UParams& up, const float* part, const float* plb, const float* pmb,
                        uint64_t* part_full, uint64_t* part_empty, const URec* rinfo, float* ust, URec* uhdr,
-                       uint64_t* ufull, uint64_t* uempty, Ctrl* ctrl) {
+                       uint64_t* ufull, uint64_t* uempty, uint64_t* ustart, Ctrl* ctrl) {
     constexpr int G = C::GQ, SPL = C::SPL, RGW = C::RGW, W = SPL + 2;
     constexpr int UBUF = kUnitBlocks * kUnitWords * 32;  // floats of one summary buffer
     constexpr int NPR = C::RGW * C::PRW;  // partial rows per record
@@ -1067,10 +1067,20 @@ __device__ void summ_u(const Params& p, const UParams& up, const float* part, co
             if (ri.kind == kUBlock && lane == 0) record_check(p.hdr, 254, ri.item, ri.k, ri.j);
             URec e = ri;
             e.kind = kUEnd;
-            if (lane == 0) uhdr[ub] = e;
+            if (lane == 0) {
+                uhdr[ub] = e;
+                uhdr[2 + ub] = e;
+            }
             __syncwarp();
             mbar_arrive_if(lane == 0, &ufull[ub]);
+            mbar_arrive_if(lane == 0, &ustart[ub]);
             return;
+        }
+        if (ri.j == 0) {
+            // the test warp may start the unit's look-back while its blocks are computed
+            if (lane == 0) uhdr[2 + ub] = ri;
+            __syncwarp();
+            mbar_arrive_if(lane == 0, &ustart[ub]);
         }
         // block max and weight sum of this lane's head over the 4 warps (each used its own
         // max), and the block's probe sums at that max
@@ -1141,7 +1151,7 @@ __device__ void summ_u(const Params& p, const UParams& up, const float* part, co
 // ---------------------------------------------------------------------------
 template <class C>
 __device__ void stat_u(const Params& p, const UParams& up, const float* ust, const URec* uhdr, uint64_t* ufull,
-                       uint64_t* uempty, Ctrl* ctrl) {
+                       uint64_t* uempty, uint64_t* ustart, Ctrl* ctrl) {
     constexpr int UBUF = kUnitBlocks * kUnitWords * 32;  // floats of one summary buffer
     bool released = false;  // the unit's summary buffer has been handed back to the summary warp
     int ub = 0;             // ... which of the two
@@ -1159,23 +1169,15 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
     probe_slots<C>(p, lane, hs, hme);
     (void)hme;
 
-    auto finish_unit = [&](int item, int k, int nj, const float* us) -> bool {
-        const size_t iu = (size_t)item * up.maxk + k;
-        // the unit's own aggregate, written by the summary warp before it handed the unit over
-        float Ma, La, Oa[SPL];
-        {
-            const float* ga = up.agg + iu * UW;
-            Ma = ga[lane];
-            La = ga[32 + lane];
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) Oa[j] = ga[(2 + j) * 32 + lane];
-        }
-        // the probe state before this unit: aggregates of the earlier units, back to the
-        // nearest one with an inclusive state
-        float cM = -INFINITY, cL = 0.f, cO[SPL];
+    // the probe state before unit k of the item: aggregates of the earlier units, back to
+    // the nearest one with an inclusive state (dead: a unit before it was skipped, so the
+    // item stopped before it). Taken when the unit starts, while its blocks are computed.
+    auto lookback = [&](int item, int k, float& cM, float& cL, float (&cO)[SPL], bool& dead) -> bool {
+        cM = -INFINITY;
+        cL = 0.f;
 #pragma unroll
         for (int j = 0; j < SPL; ++j) cO[j] = 0.f;
-        bool dead = false;
+        dead = false;
         {
             // lane j reads the flag of unit kk - j; the lanes from 0 up to the first unit with an
             // inclusive state (or a skip mark, or the list's start) whose states are published
@@ -1238,19 +1240,46 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
                 kk -= take;
             }
         }
+        return true;
+    };
+
+    // until every block of buffer ub's unit (item, k) is summarized and its aggregate written
+    auto wait_unit = [&](int uu, int item, int k) -> bool {
+        if (!wait_bounded(&ufull[ub], (uint32_t)(uu >> 1) & 1u, ctrl, p.hdr, 251)) return false;
+        const URec ri = uhdr[ub];
+        if (ri.kind != kUBlock || ri.item != item || ri.k != k) {
+            if (lane == 0) record_check(p.hdr, 257, ri.item, ri.k, k);
+            return false;
+        }
+        return true;
+    };
+
+    auto finish_unit = [&](int uu, int item, int k, int nj, float cM, float cL, const float (&cO)[SPL],
+                           bool dead) -> bool {
+        const size_t iu = (size_t)item * up.maxk + k;
+        const float* us = ust + (size_t)ub * UBUF;
         int* uf = up.uflags + 4 * iu;
         if (dead) {
+            if (!wait_unit(uu, item, k)) return false;
             if (lane == 0) {
                 st_release_gpu(&up.tflag[iu], 3);
                 st_release_gpu(uf + 2, 3);
             }
         } else {
+            if (!wait_unit(uu, item, k)) return false;
             {
+                // the unit's own aggregate, written by the summary warp before it handed the
+                // unit over, and the inclusive state (its flag follows after the first pass)
+                float Ma, La, Oa[SPL];
+                const float* ga = up.agg + iu * UW;
+                Ma = ga[lane];
+                La = ga[32 + lane];
+#pragma unroll
+                for (int j = 0; j < SPL; ++j) Oa[j] = ga[(2 + j) * 32 + lane];
                 float iM = cM, iL = cL, iO[SPL];
 #pragma unroll
                 for (int j = 0; j < SPL; ++j) iO[j] = cO[j];
                 state_merge<SPL>(iM, iL, iO, Ma, La, Oa);
-                // its flag follows after the tests' first pass, when these stores are done
                 float* gi = up.incl + iu * UW;
                 gi[lane] = iM;
                 gi[32 + lane] = iL;
@@ -1396,11 +1425,16 @@ __device__ void stat_u(const Params& p, const UParams& up, const float* ust, con
 
     for (int uu = 0;; ++uu) {
         ub = uu & 1;
-        if (!wait_bounded(&ufull[ub], (uint32_t)(uu >> 1) & 1u, ctrl, p.hdr, 251)) return;
-        const URec ri = uhdr[ub];
-        if (ri.kind != kUBlock) return;
+        // the unit that started in buffer ub: its look-back, then (once its blocks are
+        // summarized) its tests
+        if (!wait_bounded(&ustart[ub], (uint32_t)(uu >> 1) & 1u, ctrl, p.hdr, 256)) return;
+        const URec rs = uhdr[2 + ub];
+        if (rs.kind != kUBlock) return;
         released = false;
-        const bool done = finish_unit(ri.item, ri.k, ri.nj, ust + (size_t)ub * UBUF);
+        float cM, cL, cO[SPL];
+        bool dead;
+        if (!lookback(rs.item, rs.k, cM, cL, cO, dead)) return;
+        const bool done = finish_unit(uu, rs.item, rs.k, rs.nj, cM, cL, cO, dead);
         release_buffer();  // a unit whose item had stopped before it has not read its summaries
         if (!done) return;
     }
@@ -1430,6 +1464,7 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
     uint64_t* uempty = ufull + 2;              // [2]
     uint64_t* stall_bar = uempty + 2;  // never completed (the failure-path test hook)
     uint64_t* qfree = stall_bar + 1;    // [2]: the consumers are done with a query tile
+    uint64_t* ustart = qfree + 2;       // [2]: a unit has started in summary buffer 0 / 1
     float* ust = up.ustore + (size_t)blockIdx.x * 2 * kUnitBlocks * kUnitWords * 32;  // this CTA's summary store
     int* prank = reinterpret_cast<int*>(smem + L.ptab);
     URec* rinfo = reinterpret_cast<URec*>(smem + L.rinfo);
@@ -1451,6 +1486,8 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
         mbar_init(stall_bar, 1);
         mbar_init(&qfree[0], C::GW);
         mbar_init(&qfree[1], C::GW);
+        mbar_init(&ustart[0], 1);
+        mbar_init(&ustart[1], 1);
         ctrl->stop_item = -1;
         ctrl->abort = 0;
         ctrl->wait_ns = p.wait_ns;
@@ -1480,10 +1517,10 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
         if (kART)
             summ_u<C>(p, up, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
                       reinterpret_cast<const float*>(smem + L.pmb), part_full, part_empty, rinfo,
-                      ust, reinterpret_cast<URec*>(smem + L.uhdr), ufull, uempty, ctrl);
+                      ust, reinterpret_cast<URec*>(smem + L.uhdr), ufull, uempty, ustart, ctrl);
     } else if (warp == 6) {
         if (kART)
-            stat_u<C>(p, up, ust, reinterpret_cast<const URec*>(smem + L.uhdr), ufull, uempty, ctrl);
+            stat_u<C>(p, up, ust, reinterpret_cast<const URec*>(smem + L.uhdr), ufull, uempty, ustart, ctrl);
     } else {
         consumer_u<C, UC, kART>(p, up, ring, meta, full, empty, part_full, part_empty, qfree, rinfo, L, smem, prank,
                                 ctrl);
@@ -1492,25 +1529,32 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
 
 // Per (item, query head): merge the partials of the units before the stopping unit and
 // of the fix pieces (or of the stopping unit itself when it ends at the stop), and write
-// O = sums / weight sums and blocks_used. Thread d holds head dim d. The partials' maxima
-// and weight sums are first loaded into shared memory together (one load each, spread
-// over the threads), reduced to the common max and the weight sum, and turned into
-// factors; then each thread adds its dim's weighted sums, eight partials' loads in
-// flight at a time. The sums run in a fixed order (reproducible results).
+// O = sums / weight sums and blocks_used. The CTA's kCombineSplit x D threads first load
+// every partial's max and weight sum together (one partial per thread), reduce them to
+// the common max and the weight sum, and turn the maxima into factors; then thread
+// (s, d) adds head dim d's weighted sums of partials s, s + kCombineSplit, ..., all its
+// loads in flight at once, and the kCombineSplit sums of a dim are added in a fixed
+// order (reproducible results).
 constexpr int kCombineMax = kUnitMaxK + kUnitBlocks;  // partials of one item at most
+constexpr int kCombineSplit = 4;                      // threads per head dim
+constexpr int kCombineInFlight = 16;                  // loads of one thread in flight
 
 template <int D, int G>
-__global__ void __launch_bounds__(D) art_units_combine(const Params p, const UParams up0) {
+__global__ void __launch_bounds__(D * kCombineSplit) art_units_combine(const Params p, const UParams up0) {
     using E = Elem<true>;
+    constexpr int NT = D * kCombineSplit, NW = NT / 32;
     // launched while the unit kernel may still run: wait for it to finish
     asm volatile("griddepcontrol.wait;" ::: "memory");
     UParams up = up0;
     up.ck = p.hdr->ck;
     __shared__ float s_f[kCombineMax];  // the partials' maxima, then their factors
-    __shared__ float s_red[2][D / 32];
-    const int item = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-    const int lane = d & 31, wq = d >> 5;
-    const bool lead = threadIdx.x == 0 && h == 0;
+    __shared__ float s_l[kCombineMax];  // the partials' weight sums
+    __shared__ float s_red[2][NW];
+    __shared__ float s_sum[kCombineSplit][D];
+    const int item = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int d = tid % D, sp = tid / D;
+    const int lane = tid & 31, wq = tid >> 5;
+    const bool lead = tid == 0 && h == 0;
     const int b = item / p.Hkv, g = item - (item / p.Hkv) * p.Hkv;
     const size_t obase = ((size_t)b * p.Hq + (size_t)g * G + h) * D;
     const ItemInfo inf = p.info[item];
@@ -1519,7 +1563,7 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     const int t = n > 0 ? up.stop_min[item] : -1;
     if (bad || n == 0 || t < 0 || t >= n) {
         if (!bad && n > 0 && lead) record_check(p.hdr, 261, item, t, n);
-        E::store(p.out, obase + d, 0.f);
+        if (sp == 0) E::store(p.out, obase + d, 0.f);
         if (lead && p.blocks_used) p.blocks_used[item] = (bad || n > 0) ? -1 : 0;
         return;
     }
@@ -1539,10 +1583,12 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     auto o_of = [&](int q) -> const float* {
         return q < nunits ? up.part_o + (ubase + q) * G * D : up.fix_o + (fbase + q) * G * D;
     };
-    // the common max
+    // the common max (the weight sums are loaded with the maxima)
     float mx = -INFINITY;
-    for (int q = d; q < nq; q += D) {
-        const float m = __ldcg(ml_of(q) + h);
+    for (int q = tid; q < nq; q += NT) {
+        const float* ml = ml_of(q);
+        const float m = __ldcg(ml + h);
+        s_l[q] = __ldcg(ml + 8 + h);
         s_f[q] = m;
         mx = fmaxf(mx, m);
     }
@@ -1552,14 +1598,14 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     __syncthreads();
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) M = fmaxf(M, s_red[0][w]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_red[0][w]);
     // factors and the weight sum
     float den = 0.f;
-    for (int q = d; q < nq; q += D) {
+    for (int q = tid; q < nq; q += NT) {
         const float m = s_f[q];
         const float f = m == -INFINITY ? 0.f : exp2f(m - M);
         s_f[q] = f;
-        den = fmaf(f, __ldcg(ml_of(q) + 8 + h), den);
+        den = fmaf(f, s_l[q], den);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -1567,19 +1613,30 @@ __global__ void __launch_bounds__(D) art_units_combine(const Params p, const UPa
     __syncthreads();
     float L = 0.f;
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) L += s_red[1][w];
-    // this dim's weighted sums
+    for (int w = 0; w < NW; ++w) L += s_red[1][w];
+    // this thread's share of dim d's weighted sums: partials sp, sp + kCombineSplit, ...
     float num = 0.f;
-    int q = 0;
-    for (; q + 8 <= nq; q += 8) {
-        float v[8];
+    for (int q0 = sp; q0 < nq; q0 += kCombineSplit * kCombineInFlight) {
+        float v[kCombineInFlight];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) v[x] = __ldcg(o_of(q + x) + h * D + d);
+        for (int x = 0; x < kCombineInFlight; ++x) {
+            const int q = q0 + x * kCombineSplit;
+            v[x] = q < nq ? __ldcg(o_of(q) + h * D + d) : 0.f;
+        }
 #pragma unroll
-        for (int x = 0; x < 8; ++x) num = fmaf(s_f[q + x], v[x], num);
+        for (int x = 0; x < kCombineInFlight; ++x) {
+            const int q = q0 + x * kCombineSplit;
+            if (q < nq) num = fmaf(s_f[q], v[x], num);
+        }
     }
-    for (; q < nq; ++q) num = fmaf(s_f[q], __ldcg(o_of(q) + h * D + d), num);
-    E::store(p.out, obase + d, num / L);
+    s_sum[sp][d] = num;
+    __syncthreads();
+    if (sp == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCombineSplit; ++k) tot += s_sum[k][d];
+        E::store(p.out, obase + d, tot / L);
+    }
 }
 
 // Largest ring depth (2..8 slots) that lets `want` CTAs share one SM.
@@ -1653,7 +1710,7 @@ cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(p.num_items, G, 1);
-    cfg.blockDim = dim3(D);
+    cfg.blockDim = dim3(D * kCombineSplit);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
