@@ -2156,13 +2156,13 @@ __global__ void __launch_bounds__(C::THREADS, (MinBlocks<C>::value))
     if (p.stall && warp < NWC && !wait_bounded(stall_bar, 0u, ctrl, p.hdr, 161)) return;
     if (warp == NWC) {
         producer_warp<C, kART>(p, ring, meta, job, full, empty, jobb, ctrl, &tk, &tv);
-    } else if (C::COPYW && warp >= NWC + 2) {
-        copy_warp<C>(p, ring, job, last_entry, full, jobb, ctrl, &tk, &tv, warp - (NWC + 2));
     } else if (warp == NWC + 1) {
         if (kART)
             stat_warp<C>(p, reinterpret_cast<const float*>(smem + L.part), reinterpret_cast<const float*>(smem + L.plb),
                          reinterpret_cast<const float*>(smem + L.pmb), reinterpret_cast<float*>(smem + L.sh),
                          part_full, dec_bar, ctrl);
+    } else if (warp >= NWC + 2) {  // the copy warps (none without COPYW)
+        if constexpr (C::COPYW) copy_warp<C>(p, ring, job, last_entry, full, jobb, ctrl, &tk, &tv, warp - (NWC + 2));
     } else if constexpr (C::TC) {
         if constexpr (C::DS)
             consumer_ds<C, kART>(p, ring, meta, full, empty, part_full, dec_bar, cbar, L, smem, prank, ctrl);
@@ -2241,7 +2241,7 @@ cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, Laun
     const int want = MinBlocks<C>::value < per_sm ? MinBlocks<C>::value : per_sm;
     int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(want, smem_sm, smem_blk);
     if (stages == 0) stages = pick_stages<C>(1, smem_sm, smem_blk);
-    if (C::NCW > 1) stages -= stages % C::NCW;  // every slot's entries go to one copy warp
+    if constexpr (C::NCW > 1) stages -= stages % C::NCW;  // every slot's entries go to one copy warp
     if (stages < 2) return cudaErrorInvalidConfiguration;
     const size_t smem = make_layout<C>(stages).total;
     if ((int)smem > smem_blk) return cudaErrorInvalidConfiguration;
