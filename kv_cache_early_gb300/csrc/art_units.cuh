@@ -1535,7 +1535,6 @@ __global__ void __launch_bounds__(UCfg<D, G>::THREADS, 2)
 // (s, d) adds head dim d's weighted sums of partials s, s + kCombineSplit, ..., all its
 // loads in flight at once, and the kCombineSplit sums of a dim are added in a fixed
 // order (reproducible results).
-constexpr int kCombineMax = kUnitMaxK + kUnitBlocks;  // partials of one item at most
 constexpr int kCombineSplit = 4;                      // threads per head dim
 constexpr int kCombineInFlight = 16;                  // loads of one thread in flight
 
@@ -1547,8 +1546,9 @@ __global__ void __launch_bounds__(D * kCombineSplit) art_units_combine(const Par
     asm volatile("griddepcontrol.wait;" ::: "memory");
     UParams up = up0;
     up.ck = p.hdr->ck;
-    __shared__ float s_f[kCombineMax];  // the partials' maxima, then their factors
-    __shared__ float s_l[kCombineMax];  // the partials' weight sums
+    extern __shared__ float s_dyn[];
+    float* s_f = s_dyn;                          // [maxk + kUnitBlocks] the partials' maxima, then factors
+    float* s_l = s_dyn + up0.maxk + kUnitBlocks;  // [maxk + kUnitBlocks] the partials' weight sums
     __shared__ float s_red[2][NW];
     __shared__ float s_sum[kCombineSplit][D];
     const int item = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -1572,8 +1572,8 @@ __global__ void __launch_bounds__(D * kCombineSplit) art_units_combine(const Par
     const bool use_fix = t != min(n, sfirst + up.ck) - 1;
     const int nunits = use_fix ? kk : kk + 1;                // whole units
     const int nq = nunits + (use_fix ? t - sfirst + 1 : 0);  // ... then fix pieces (one block each)
-    if (nq > kCombineMax) {  // beyond the workspace's sizing: cannot happen for a checked plan
-        if (lead) record_check(p.hdr, 263, item, nq, kCombineMax);
+    if (nq > up.maxk + kUnitBlocks) {  // beyond the workspace's sizing: cannot happen for a checked plan
+        if (lead) record_check(p.hdr, 263, item, nq, up.maxk + kUnitBlocks);
         return;
     }
     const size_t ubase = (size_t)item * up.maxk, fbase = (size_t)item * up.ck - nunits;
@@ -1711,7 +1711,8 @@ cudaError_t launch_units(Params p, UParams up, cudaStream_t stream, LaunchInfo* 
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(p.num_items, G, 1);
     cfg.blockDim = dim3(D * kCombineSplit);
-    cfg.dynamicSmemBytes = 0;
+    // the partials' maxima and weight sums: up to maxk units and kUnitBlocks fix pieces
+    cfg.dynamicSmemBytes = (size_t)2 * (up.maxk + kUnitBlocks) * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
