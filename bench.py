@@ -431,6 +431,21 @@ def run_ours(args):
                 "units" if art_on_units else "one CTA per item")
         if "fastest_dense_ms_per_step" in dense:
             dense["art_eps0_over_fastest_dense"] = ms_z / dense["fastest_dense_ms_per_step"]
+        # with selected lists shorter than the context (the long-context workload), the
+        # full scan of the whole cache too: what key selection plus ART replaces
+        if w.visit_order is not None and int(w.visit_lengths().sum()) < int(np.ceil(w.seq_lens / w.block_size).sum()) * w.num_kv_heads:
+            full = lambda: dev.dense(stream=stream, visit_order=None)
+            for _ in range(3):
+                full()
+            t_f, t_fk = time_calls(full, args.steps, kernel=True)
+            ms_f, ms_fk = float(t_f.mean()), float(t_fk.mean())
+            full_bytes = int(w.seq_lens.sum()) * w.num_kv_heads * 2 * w.head_dim * w.elem_bytes
+            dense["full_cache"] = {
+                "what": "the dense twin over every block of the cache in natural order (NULL lists)",
+                "ms_per_step": ms_f, "kernel_ms": ms_fk,
+                "path": "units" if K.dense_decode_path(dev.shape, dev.workspace.numel()) == 1 else "one CTA per item",
+                "kv_bytes": full_bytes, "kernel_gbs": full_bytes / (ms_fk * 1e-3) / 1e9,
+                "speedup_art_over_full_cache": ms_f / ms}
 
     # roofline of the decode kernel (bytes actually needed by the blocks processed)
     path = K.art_decode_path(dev.shape, p, dev.workspace.numel())
