@@ -28,6 +28,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -182,11 +183,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
+def _code_only(src: bytes) -> bytes:
+    """Source text without comments and blank lines (comments do not change a kernel)."""
+    t = re.sub(r"/\*.*?\*/", "", src.decode(), flags=re.S)
+    t = re.sub(r"//[^\n]*", "", t)
+    return "\n".join(line.rstrip() for line in t.splitlines() if line.strip()).encode()
+
+
 def kernel_source_hash(path=None):
-    """Hash of the CUDA sources a kernel path compiles from: "one CTA per item"
-    (the decode kernel, its instantiations and the plan kernel), "units" (the
-    unit and merge kernels, which also use the decode kernel's helpers), or
-    every source when path is None."""
+    """Hash of the code (comments stripped) of the CUDA sources a kernel path
+    compiles from: "one CTA per item" (the decode kernel, its instantiations and
+    the plan kernel), "units" (the unit and merge kernels, which also use the
+    decode kernel's helpers), or every source when path is None."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_early_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
@@ -198,7 +206,7 @@ def kernel_source_hash(path=None):
             continue
         if path == "units" and f.startswith("art_inst_"):
             continue
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f), "rb").read()))
     return h.hexdigest()[:16]
 
 

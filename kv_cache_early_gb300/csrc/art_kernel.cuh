@@ -1,16 +1,24 @@
 // art_kernel.cuh -- the persistent, warp-specialized ART decode-attention kernel.
 //
-// One CTA runs three roles over a ring of shared-memory slots, each slot
+// One CTA runs these roles over a ring of shared-memory slots, each slot
 // holding one 64-token ART block of K rows, V rows and (with a consumer
 // group's first block of an item) the item's G query vectors:
 //
 //   producer warp    claims work items (sequence b, KV head g) in the order the
-//                    plan kernel wrote (longest visit list first), resolves
+//                    plan kernel wrote (longest visit list first) and resolves
 //                    visit entry -> logical block -> physical pages through the
-//                    block table, and fills slots with TMA copies (bf16: one
-//                    3-D tensor copy per page; fp32: one bulk copy per page)
-//                    that complete on the slot's mbarrier. It stops issuing an
-//                    item's blocks once the statistics warp has stopped it.
+//                    block table. For each ring entry it waits for the slot and
+//                    writes the slot's metadata; with copy warps it posts a copy
+//                    job (the pages' rows in the tensor maps), otherwise it
+//                    issues the copies itself (fp32: one bulk copy per page).
+//                    It posts no more blocks of an item once the statistics
+//                    warp has stopped it.
+//   copy warps       (bf16, one CTA per SM) take alternate ring entries, arm the
+//                    slot's mbarrier with the entry's bytes and issue its copies
+//                    (one 3-D tensor copy per page of K and of V, and the
+//                    queries). A tensor copy holds the issuing warp until the
+//                    copy engine accepts it, so issuing apart from resolving
+//                    lets the two overlap.
 //   consumer warps   softmax attention of the block for the item's G query
 //                    heads and the online-softmax fold into running
 //                    accumulators (ART paper sec. 3.1: FlashAttention's
@@ -18,8 +26,8 @@
 //                    - fp32: 8 warps on CUDA cores (packed f32x2 FMA), each
 //                      owning 8 of the block's rows;
 //                    - bf16, groups of 4 warps with the head dims split: three
-//                      groups by default, or one for a probe over more than 32
-//                      columns per head;
+//                      groups by default, four when each CTA runs one item,
+//                      or one for a probe over more than 32 columns per head;
 //                    - bf16, one or two groups of 4 warps with the keys split
 //                      (when forced with ART_GROUPS).
 //                    Several groups of one CTA take alternate blocks of the
@@ -43,8 +51,8 @@
 // |x_i/|x_i| - x_{i-1}/|x_{i-1}||^2 / 2.
 //
 // Every mbarrier wait is bounded (Params::wait_ns, 1 s); on expiry the kernel
-// sets ART_STATUS_TIMEOUT, the producer waits for its own copies in flight,
-// and the CTA returns.
+// sets ART_STATUS_TIMEOUT, the warps that issued copies wait for their own
+// copies in flight, and the CTA returns.
 #pragma once
 
 #include <cstddef>
