@@ -2,12 +2,13 @@
 
 Every wait in the kernels (mbarrier phases, flags written by other CTAs) is
 bounded: when one runs out, the kernel sets ART_STATUS_TIMEOUT in the
-workspace, each warp gives up at its own bounded wait, the producer waits for
-its own copies in flight, and the CTA returns, leaving the context usable.
+workspace, each warp gives up at its own bounded wait, the warps that issued
+copies wait for their own copies in flight, and the CTA returns, leaving the
+context usable.
 
 The test hook ART_TEST_STALL_NS=<ns> makes the consumer warps first wait on a
-barrier that nothing completes, and sets every wait limit to <ns> (the
-producer's final drain of its copies keeps its 1 s limit). The call must
+barrier that nothing completes, and sets every wait limit to <ns> (the final
+drain of a warp's own copies keeps its 1 s limit). The call must
 return, the stream synchronize without a CUDA error, the status word carry the
 timeout bit, and the next call with the hook off, on the same buffers, must
 match the oracle.
@@ -25,10 +26,16 @@ TIMEOUT_BIT = 32  # ART_STATUS_TIMEOUT
 
 
 @pytest.mark.parametrize("mode", ["art", "dense"])
-@pytest.mark.parametrize("k,path", [(2, "one-cta"), (2, "units"), (3, "units"), (1, "one-cta")])
-def test_bounded_wait_expires_and_next_call_is_clean(k, path, mode, monkeypatch):
+@pytest.mark.parametrize("k,path,groups", [
+    (2, "one-cta", None),  # four consumer groups and one copy warp (items fit one per SM)
+    (2, "one-cta", "3"),   # three groups and two copy warps
+    (2, "one-cta", "1"),   # one keys-split group, the producer issuing the copies
+    (2, "units", None), (3, "units", None), (1, "one-cta", None)])
+def test_bounded_wait_expires_and_next_call_is_clean(k, path, groups, mode, monkeypatch):
     import kv_cache_early_gb300 as K
     monkeypatch.setenv("ART_UNITS", "1" if path == "units" else "0")
+    if groups is not None:
+        monkeypatch.setenv("ART_GROUPS", groups)
     w = W.config(k, small=True)
     dev = K.DeviceInputs(w)
     assert K.art_decode_path(dev.shape, 2, dev.workspace.numel()) == (1 if path == "units" else 0)
