@@ -77,7 +77,7 @@ struct Params {
     int patience;
     int ph;  // query heads 0 .. ph-1 of a group form the probe
     // Bounded waits give up after wait_ns (kWaitLimitNs unless the test hook below is
-    // set); a producer's final drain of its own copies always allows kWaitLimitNs.
+    // set); a warp's final drain of its own copies always allows kWaitLimitNs.
     unsigned long long wait_ns;
     // Test hook of the failure path: the consumer warps first wait on a barrier that
     // nothing completes, so every warp of the CTA gives up at one of its bounded waits
