@@ -16,13 +16,15 @@
 //               output (every warp: the same running max and weight sum, the
 //               output sums of its dims), which goes to global memory at the
 //               unit's end; each block's probe partials go to the summary warp.
-//   summary     turns each block's probe partials into a block summary (max,
-//               weight sum, probe sums per head), stored per CTA in global
-//               memory, and publishes the unit's probe aggregate.
-//   tests       takes the state of the probe before the unit
-//               from a look-back over the item's earlier units (their
-//               aggregates, back to the nearest one that has published its
-//               inclusive state). From that state it runs the stability test of
+//   summary     announces each unit to the test warp when its first block's
+//               record arrives, turns each block's probe partials into a block
+//               summary (max, weight sum, probe sums per head), stored per CTA
+//               in global memory, and publishes the unit's probe aggregate.
+//   tests       takes the state of the probe before the unit from a look-back
+//               over the item's earlier units (their aggregates, back to the
+//               nearest one that has published its inclusive state), as soon as
+//               the unit is announced, while its blocks are still computed.
+//               Once the unit is summarized it runs the stability test of
 //               each block of the unit in order, exactly as one pass over the
 //               list would (ART paper sec. 3.2; explainer sec. 2.2-2.4), and
 //               publishes the unit's stable bits. With patience <= ck the
@@ -38,9 +40,11 @@
 //               block j of the stopping unit if it lies at or before the stop
 //               (that unit's own partial also holds blocks after it), one block
 //               per CTA, so the recompute is spread over the GPU.
-//   combine     a second kernel merges, per item, the partials of the units
-//               before the stopping unit and of the fix pieces (or the stopping
-//               unit itself when it ends at the stop): O = sums / weight sums.
+//   combine     a second kernel (programmatic dependent launch) merges, per
+//               item and query head, the partials of the units before the
+//               stopping unit and of the fix pieces (or the stopping unit itself
+//               when it ends at the stop): O = sums / weight sums, in a fixed
+//               order.
 //
 // A unit whose item has already stopped before it when it is claimed is
 // skipped; units claimed before the stop was known are read and discarded.
