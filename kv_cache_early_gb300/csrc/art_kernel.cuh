@@ -2250,7 +2250,10 @@ cudaError_t launch_variant(Params p, cudaStream_t stream, int force_stages, Laun
     int stages = force_stages >= 2 && force_stages <= 8 ? force_stages : pick_stages<C>(want, smem_sm, smem_blk);
     if (stages == 0) stages = pick_stages<C>(1, smem_sm, smem_blk);
     if constexpr (C::NCW > 1) stages -= stages % C::NCW;  // every slot's entries go to one copy warp
-    if (stages < 2) return cudaErrorInvalidConfiguration;
+    // At an item's end each group merges while it holds the slot of its first entry of
+    // the next item, so all NG such entries must fit in the ring at once.
+    constexpr int kMinStages = C::NG < 2 ? 2 : (C::NCW > 1 ? (C::NG + C::NCW - 1) / C::NCW * C::NCW : C::NG);
+    if (stages < kMinStages) stages = kMinStages;
     const size_t smem = make_layout<C>(stages).total;
     if ((int)smem > smem_blk) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)

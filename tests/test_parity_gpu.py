@@ -266,6 +266,28 @@ def test_consumer_group_variants(small, k, groups, monkeypatch):
     check_dense(w, out, what=f"dense config {k} groups {groups}")
 
 
+@pytest.mark.parametrize("groups,stages", [("3", "2"), ("3", "3"), ("3", "5"), ("4", "3"), ("2", "3")])
+def test_ring_depths(small, groups, stages, monkeypatch):
+    """Shallow and odd ring depths (ART_STAGES): the library raises the depth to
+    one slot per consumer group (at an item's end every group merges while holding
+    its first entry of the next item) and, with two copy warps (three groups),
+    rounds it to an even count so that each slot's entries stay with one copy
+    warp. Every depth must give the oracle's result, ART and dense, over repeated
+    calls."""
+    monkeypatch.setenv("ART_GROUPS", groups)
+    monkeypatch.setenv("ART_STAGES", stages)
+    monkeypatch.setenv("ART_UNITS", "0")
+    w = small[4]
+    dev = None
+    for _ in range(2):
+        out, bu, st, dev = run_gpu(w, "art", 1e-2, 1e-2, 2, dev=dev)
+        assert st == 0
+        check_art(w, out, bu, 1e-2, 1e-2, 2, what=f"ring depth {stages}, groups {groups}")
+    out, _, st, _ = run_gpu(w, "dense", dev=dev)
+    assert st == 0
+    check_dense(w, out, what=f"dense, ring depth {stages}, groups {groups}")
+
+
 @pytest.mark.parametrize("groups", ["2", "3", "4"])
 def test_many_short_items_multi_group(groups, monkeypatch):
     """Hundreds of short items per call: with several consumer groups the ring
