@@ -13,6 +13,25 @@ namespace art {
 template <bool kBF16, int D, int G, bool kART>
 cudaError_t launch_main(Params p, cudaStream_t stream, int force_stages, LaunchInfo* li);
 
+// The kernels are compiled in their own translation units (art_inst_*.cu,
+// art_units_d*.cu); here they are only called.
+#define ART_EXTERN_MAIN(BF, D, G)                                                                      \
+    extern template cudaError_t launch_main<BF, D, G, true>(Params, cudaStream_t, int, LaunchInfo*); \
+    extern template cudaError_t launch_main<BF, D, G, false>(Params, cudaStream_t, int, LaunchInfo*);
+#define ART_EXTERN_UNITS(D, G)                                                                        \
+    extern template cudaError_t launch_units<D, G, true>(Params, UParams, cudaStream_t, LaunchInfo*); \
+    extern template cudaError_t launch_units<D, G, false>(Params, UParams, cudaStream_t, LaunchInfo*);
+#define ART_EXTERN_ALL_G(M, ...) M(__VA_ARGS__, 1) M(__VA_ARGS__, 2) M(__VA_ARGS__, 4) M(__VA_ARGS__, 7) M(__VA_ARGS__, 8)
+ART_EXTERN_ALL_G(ART_EXTERN_MAIN, true, 128)
+ART_EXTERN_ALL_G(ART_EXTERN_MAIN, true, 64)
+ART_EXTERN_ALL_G(ART_EXTERN_MAIN, false, 128)
+ART_EXTERN_ALL_G(ART_EXTERN_MAIN, false, 64)
+ART_EXTERN_ALL_G(ART_EXTERN_UNITS, 128)
+ART_EXTERN_ALL_G(ART_EXTERN_UNITS, 64)
+#undef ART_EXTERN_ALL_G
+#undef ART_EXTERN_UNITS
+#undef ART_EXTERN_MAIN
+
 constexpr int kPlanThreads = 256;
 constexpr int kBitmapWords = 2048;  // duplicate detection for lists over up to 65536 blocks
 constexpr int kSortBuckets = 4096;  // LPT bucketing of visit-list lengths
